@@ -1,0 +1,175 @@
+/*
+ * flint_moe.h -- C ABI of the GB300 (sm_103a) Flint MoE sublayer library.
+ *
+ * The operation is the MoE sublayer of the Flint model as described in
+ * "Day-0 Support for Flint on vLLM" (sections "Model architecture" and
+ * "Optimizations"): a 2048-wide token x_hat is scored by a bf16 router over
+ * 256 experts, the 6 experts with the largest sigmoid score are selected and
+ * their scores renormalised to sum to 1, each selected expert and the
+ * always-on shared expert compute down(bf16(silu(gate(x_hat)) * up(x_hat))),
+ * and the outputs are combined with the routing weights (shared weight 1) and
+ * rounded once to bf16.  Expert weights are NVFP4 (16 E2M1 codes + one E4M3
+ * block scale per 16 weights + one fp32 per-tensor scale) used weight-only
+ * with bf16 activations ("W4A16", same section), or plain bf16.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers (the current CUDA device) owned
+ *     by the caller; every pointer must be 16-byte aligned.  Row-major layouts.
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns a negative status and enqueues nothing.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream); outputs are valid after the stream is synchronised.
+ *   - The library allocates no device memory on the compute path: scratch
+ *     space is the caller's workspace `ws` (size from flint_moe_workspace_bytes,
+ *     256-byte aligned, no initialisation needed).  Calls that share one
+ *     workspace must be ordered on one stream.
+ *   - Only the Flint shapes are supported: hidden 2048, 256 routed experts,
+ *     1 shared expert, intermediate 512, top-6.  Anything else returns
+ *     FLINT_MOE_ERR_UNSUPPORTED (there is no generic fallback path).
+ */
+#ifndef FLINT_MOE_H
+#define FLINT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's stream handle type). */
+typedef struct CUstream_st *flint_moe_stream_t;
+
+/* Status codes returned by every int-returning entry point. */
+enum {
+    FLINT_MOE_OK = 0,
+    FLINT_MOE_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad count  */
+    FLINT_MOE_ERR_UNSUPPORTED = -2, /* shape or batch outside the fast path */
+    FLINT_MOE_ERR_WORKSPACE = -3,   /* workspace or output buffer too small */
+    FLINT_MOE_ERR_CUDA = -4,        /* a CUDA runtime call failed           */
+    FLINT_MOE_ERR_TIMEOUT = -5      /* a bounded device wait gave up        */
+};
+
+/* Expert weight formats. */
+enum { FLINT_MOE_W_NVFP4 = 0, FLINT_MOE_W_BF16 = 1 };
+
+/* Largest batch of the low-latency decode path ("Optimizations": the
+ * low-latency path serves up to 8 requests). */
+#define FLINT_MOE_MAX_DECODE_BATCH 8
+
+/* Model dimensions.  Must equal {2048, 256, 1, 512, 6, *, eps}. */
+typedef struct {
+    int hidden;       /* H = 2048                                   */
+    int n_experts;    /* E = 256 routed experts                     */
+    int n_shared;     /* 1 shared expert (index E in the blobs)     */
+    int inter;        /* I = 512 expert intermediate size           */
+    int top_k;        /* 6                                          */
+    int weight_dtype; /* FLINT_MOE_W_NVFP4 or FLINT_MOE_W_BF16      */
+    float rms_eps;    /* RMSNorm epsilon (1e-6 for Flint stacks)    */
+} flint_moe_dims;
+
+/* One MoE sublayer's weights (all device pointers, caller-owned). */
+typedef struct {
+    const void *router_w;       /* bf16 [E][H]                                   */
+    const void *experts;        /* packed blob from flint_moe_pack_weights       */
+    const float *tensor_scales; /* NVFP4: fp32 [E+1][2] = (gate/up, down) scale
+                                   per expert; ignored (may be NULL) for BF16    */
+    const void *norm_w;         /* bf16 [H] RMSNorm weight applied to this
+                                   sublayer's input, or NULL for no norm         */
+} flint_moe_layer;
+
+/* Bytes of one sublayer's packed expert blob (E routed + 1 shared expert):
+ * NVFP4 1,769,472 B per expert, BF16 6,291,456 B per expert (the same byte
+ * count as the plain layout: the repack is lossless and adds no padding).
+ * Returns 0 for unsupported dims. */
+size_t flint_moe_packed_bytes(const flint_moe_dims *dims);
+
+/* Workspace bytes for calls with at most `max_tokens` tokens
+ * (decode: 1..8; prefill: any T >= 1).  Returns 0 for unsupported dims. */
+size_t flint_moe_workspace_bytes(const flint_moe_dims *dims, int max_tokens);
+
+/*
+ * One-time lossless repack of one sublayer's experts from the plain layout
+ * into the kernels' interleaved layout ("Model architecture": the NVFP4
+ * checkpoint is repacked losslessly at load time).
+ *
+ * NVFP4 inputs (expert index E is the shared expert):
+ *   gate_up        uint8 [E+1][2I][H/2]  rows 0..I-1 gate, I..2I-1 up; byte j
+ *                  of a row holds element 2j in its low nibble, 2j+1 high
+ *   gate_up_scales uint8 [E+1][2I][H/16] E4M3 scale of each 16-element block
+ *   down           uint8 [E+1][H][I/2]
+ *   down_scales    uint8 [E+1][H][I/16]
+ * BF16 inputs: gate_up bf16 [E+1][2I][H], down bf16 [E+1][H][I]; the scale
+ *   pointers must be NULL.
+ * packed: output, flint_moe_packed_bytes(dims) bytes.  Runs one device kernel
+ * on `stream`; inputs may be freed once the stream has passed it.
+ */
+int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
+                           const uint8_t *gate_up_scales, const void *down,
+                           const uint8_t *down_scales, void *packed,
+                           size_t packed_bytes, flint_moe_stream_t stream);
+
+/*
+ * One MoE sublayer for a decode batch of 1..8 independent tokens.
+ *   x        bf16 [B][H] input (RMSNorm'd first if layer->norm_w != NULL)
+ *   y        bf16 [B][H] output; must not alias x
+ *   topk_ids int32 [B][6] selected experts (descending score) or NULL
+ *   topk_w   fp32  [B][6] their renormalised weights, or NULL
+ * Three kernels chained with programmatic dependent launch: the router GEMV
+ * with sigmoid top-6; the gate/up GEMV with SiLU*up over the selected experts
+ * only; the down GEMV fused with the weighted combine and the shared expert.
+ * B > 8 returns FLINT_MOE_ERR_UNSUPPORTED.
+ */
+int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
+                           const void *x, int B, void *y, int32_t *topk_ids,
+                           float *topk_w, void *ws, size_t ws_bytes,
+                           flint_moe_stream_t stream);
+
+/*
+ * n_layers chained sublayers for one decode batch: sublayer i+1 reads
+ * sublayer i's output (through its own RMSNorm when layers[i+1].norm_w is
+ * set; no residual is added).  The chain of 3*n_layers kernels is captured
+ * once into a CUDA graph (cached per argument set; see flint_moe_release) and
+ * replayed with one graph launch per call.
+ *   x, y            bf16 [B][H]; y must not alias x
+ *   ids_per_layer   int32 [n_layers][B][6] or NULL
+ *   w_per_layer     fp32  [n_layers][B][6] or NULL
+ *   ys_per_layer    bf16  [n_layers][B][H] every sublayer's output, or NULL
+ * The graph bakes in every pointer: a call with the same pointers replays the
+ * cached graph, so buffer contents may change between calls, addresses not.
+ */
+int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *layers,
+                           int n_layers, const void *x, int B, void *y,
+                           int32_t *ids_per_layer, float *w_per_layer,
+                           void *ys_per_layer, void *ws, size_t ws_bytes,
+                           flint_moe_stream_t stream);
+
+/*
+ * One MoE sublayer over T tokens (prefill shape, e.g. T = 8192): router GEMM
+ * with top-6, tokens grouped by expert, grouped gate/up GEMM with SiLU*up and
+ * grouped down GEMM on the tensor cores, weighted combine plus shared expert.
+ *   x bf16 [T][H], y bf16 [T][H], topk_ids int32 [T][6] / topk_w fp32 [T][6]
+ *   or NULL.  NVFP4 weights only.
+ */
+int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
+                            const void *x, int T, void *y, int32_t *topk_ids,
+                            float *topk_w, void *ws, size_t ws_bytes,
+                            flint_moe_stream_t stream);
+
+/* Frees cached CUDA graphs of every device the calling thread used.  Call
+ * before freeing buffers whose addresses a cached stack graph holds. */
+int flint_moe_release(void);
+
+/* Reads (and with reset != 0 clears) the current device's error word, in
+ * which a kernel records a bounded wait that gave up.  Synchronises the
+ * device.  Returns the word (0 = none) or a negative status. */
+int flint_moe_device_error(int reset);
+
+/* Static text for a status code. */
+const char *flint_moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLINT_MOE_H */

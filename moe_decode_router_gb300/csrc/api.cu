@@ -1,0 +1,300 @@
+// C ABI of the Flint MoE library: argument validation, per-device set-up, and
+// the CUDA-graph cache of the decode stack.  See include/flint_moe.h.
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <vector>
+
+#include "flint_common.cuh"
+#include "flint_internal.h"
+#include "flint_moe.h"
+
+namespace flint {
+
+// Device error word: kernels OR an error bit into it when a bounded wait
+// gives up.  Kernels get its address as a parameter.
+__device__ unsigned int g_flint_error;
+
+namespace {
+
+constexpr int MAX_GU_GRID = 512;
+constexpr size_t MAX_GRAPHS = 32;
+
+struct GraphEntry {
+  std::vector<uintptr_t> key;
+  cudaGraphExec_t exec;
+};
+
+struct DeviceState {
+  bool ready = false;
+  int sm_count = 0;
+  int gu_grid = 0;
+  unsigned* err = nullptr;
+  cudaStream_t capture_stream = nullptr;
+  std::vector<GraphEntry> graphs;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_devices;
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA; }
+
+// Called with g_mu held.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (major != 10) return FLINT_MOE_ERR_UNSUPPORTED;  // built for sm_103a only
+    s.gu_grid = s.sm_count < MAX_GU_GRID ? s.sm_count : MAX_GU_GRID;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_flint_error) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&s.capture_stream, cudaStreamNonBlocking) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    s.ready = true;
+  }
+  *out = &s;
+  return FLINT_MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(const flint_moe_dims* d) {
+  if (d == nullptr) return FLINT_MOE_ERR_INVALID_ARG;
+  if (d->hidden != H || d->n_experts != E || d->n_shared != 1 || d->inter != I || d->top_k != TOPK)
+    return FLINT_MOE_ERR_UNSUPPORTED;
+  if (d->weight_dtype != FLINT_MOE_W_NVFP4 && d->weight_dtype != FLINT_MOE_W_BF16) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (!(d->rms_eps >= 0.f) || !std::isfinite(d->rms_eps)) return FLINT_MOE_ERR_INVALID_ARG;
+  return FLINT_MOE_OK;
+}
+
+int check_layer(const flint_moe_dims* d, const flint_moe_layer* L) {
+  if (L == nullptr || L->router_w == nullptr || L->experts == nullptr) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(L->router_w, 16) || !aligned(L->experts, 16)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (d->weight_dtype == FLINT_MOE_W_NVFP4 && (L->tensor_scales == nullptr || !aligned(L->tensor_scales, 16)))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (L->norm_w != nullptr && !aligned(L->norm_w, 16)) return FLINT_MOE_ERR_INVALID_ARG;
+  return FLINT_MOE_OK;
+}
+
+bool opt_aligned(const void* p) { return p == nullptr || aligned(p, 16); }
+
+LayerArgs layer_args(const flint_moe_layer& L) {
+  LayerArgs a;
+  a.router_w = L.router_w;
+  a.experts = static_cast<const uint8_t*>(L.experts);
+  a.tscale = L.tensor_scales;
+  a.norm_w = L.norm_w;
+  return a;
+}
+
+size_t decode_ws_needed() { return decode_ws_bytes(MAX_GU_GRID); }
+
+}  // namespace
+}  // namespace flint
+
+using namespace flint;
+
+extern "C" {
+
+size_t flint_moe_packed_bytes(const flint_moe_dims* dims) {
+  if (check_dims(dims) != FLINT_MOE_OK) return 0;
+  return (size_t)NE * (dims->weight_dtype == FLINT_MOE_W_NVFP4 ? F4_EXPERT : B16_EXPERT);
+}
+
+size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int max_tokens) {
+  if (check_dims(dims) != FLINT_MOE_OK || max_tokens < 1) return 0;
+  if (max_tokens <= BMAX) return decode_ws_needed();
+  return 0;  // prefill workspace: not available in this build
+}
+
+int flint_moe_pack_weights(const flint_moe_dims* dims, const void* gate_up, const uint8_t* gate_up_scales,
+                           const void* down, const uint8_t* down_scales, void* packed, size_t packed_bytes,
+                           flint_moe_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != FLINT_MOE_OK) return st;
+  const bool f4 = dims->weight_dtype == FLINT_MOE_W_NVFP4;
+  if (gate_up == nullptr || down == nullptr || packed == nullptr) return FLINT_MOE_ERR_INVALID_ARG;
+  if (f4 && (gate_up_scales == nullptr || down_scales == nullptr)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!f4 && (gate_up_scales != nullptr || down_scales != nullptr)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(gate_up, 16) || !aligned(down, 16) || !aligned(packed, 16) || !opt_aligned(gate_up_scales) ||
+      !opt_aligned(down_scales))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (packed_bytes < flint_moe_packed_bytes(dims)) return FLINT_MOE_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+  return to_status(launch_pack(f4 ? 0 : 1, gate_up, gate_up_scales, down, down_scales, packed,
+                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int flint_moe_decode_layer(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int B, void* y,
+                           int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, flint_moe_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != FLINT_MOE_OK) return st;
+  if ((st = check_layer(dims, layer)) != FLINT_MOE_OK) return st;
+  if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (B > BMAX) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (x == nullptr || y == nullptr || ws == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+  const DecodeWs w = carve_decode_ws(ws, MAX_GU_GRID);
+  return to_status(launch_decode_layer(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, layer_args(*layer), x,
+                                       nullptr, B, dims->rms_eps, y, nullptr, nullptr, topk_ids, topk_w, w,
+                                       ds->gu_grid, ds->err, reinterpret_cast<cudaStream_t>(stream), true));
+}
+
+int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* layers, int n_layers, const void* x,
+                           int B, void* y, int32_t* ids_per_layer, float* w_per_layer, void* ys_per_layer, void* ws,
+                           size_t ws_bytes, flint_moe_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != FLINT_MOE_OK) return st;
+  if (layers == nullptr || n_layers < 1 || n_layers > 4096) return FLINT_MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_layers; ++i)
+    if ((st = check_layer(dims, &layers[i])) != FLINT_MOE_OK) return st;
+  if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (B > BMAX) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (x == nullptr || y == nullptr || ws == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(ids_per_layer) ||
+      !opt_aligned(w_per_layer) || !opt_aligned(ys_per_layer))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+
+  std::vector<uintptr_t> key;
+  key.reserve(16 + 4 * (size_t)n_layers);
+  key.push_back((uintptr_t)dims->weight_dtype);
+  uint32_t eps_bits;
+  std::memcpy(&eps_bits, &dims->rms_eps, 4);
+  key.push_back(eps_bits);
+  key.push_back((uintptr_t)n_layers);
+  key.push_back((uintptr_t)B);
+  key.push_back((uintptr_t)x);
+  key.push_back((uintptr_t)y);
+  key.push_back((uintptr_t)ids_per_layer);
+  key.push_back((uintptr_t)w_per_layer);
+  key.push_back((uintptr_t)ys_per_layer);
+  key.push_back((uintptr_t)ws);
+  for (int i = 0; i < n_layers; ++i) {
+    key.push_back((uintptr_t)layers[i].router_w);
+    key.push_back((uintptr_t)layers[i].experts);
+    key.push_back((uintptr_t)layers[i].tensor_scales);
+    key.push_back((uintptr_t)layers[i].norm_w);
+  }
+
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+  cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+  for (auto& ge : ds->graphs)
+    if (ge.key == key) return to_status(cudaGraphLaunch(ge.exec, user));
+
+  const int fmt = dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1;
+  const DecodeWs w = carve_decode_ws(ws, MAX_GU_GRID);
+  cudaStream_t cs = ds->capture_stream;
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  cudaError_t le = cudaSuccess;
+  for (int i = 0; i < n_layers && le == cudaSuccess; ++i) {
+    const bool last = i == n_layers - 1;
+    const void* xin = i == 0 ? x : w.y_mid;
+    void* yout = last ? y : w.y_mid;
+    // The previous sublayer's down kernel leaves the sum of squares of its
+    // output for this sublayer's RMSNorm.
+    const void* ss_in = (i > 0 && layers[i].norm_w != nullptr) ? w.ss_part : nullptr;
+    void* ss_out = (!last && layers[i + 1].norm_w != nullptr) ? w.ss_part : nullptr;
+    void* ys = ys_per_layer ? static_cast<uint8_t*>(ys_per_layer) + (size_t)i * B * H * 2 : nullptr;
+    int32_t* ids = ids_per_layer ? ids_per_layer + (size_t)i * B * TOPK : nullptr;
+    float* wl = w_per_layer ? w_per_layer + (size_t)i * B * TOPK : nullptr;
+    le = launch_decode_layer(fmt, layer_args(layers[i]), xin, ss_in, B, dims->rms_eps, yout, ys, ss_out, ids, wl, w,
+                             ds->gu_grid, ds->err, cs, true);
+  }
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(cs, &graph);
+  if (le != cudaSuccess || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return FLINT_MOE_ERR_CUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (ds->graphs.size() >= MAX_GRAPHS) {
+    cudaGraphExecDestroy(ds->graphs.front().exec);
+    ds->graphs.erase(ds->graphs.begin());
+  }
+  ds->graphs.push_back(GraphEntry{std::move(key), exec});
+  return to_status(cudaGraphLaunch(exec, user));
+}
+
+int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int T, void* y,
+                            int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, flint_moe_stream_t stream) {
+  (void)layer;
+  (void)x;
+  (void)T;
+  (void)y;
+  (void)topk_ids;
+  (void)topk_w;
+  (void)ws;
+  (void)ws_bytes;
+  (void)stream;
+  int st = check_dims(dims);
+  if (st != FLINT_MOE_OK) return st;
+  return FLINT_MOE_ERR_UNSUPPORTED;
+}
+
+int flint_moe_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  int rc = FLINT_MOE_OK;
+  for (auto& kv : g_devices) {
+    if (cudaSetDevice(kv.first) != cudaSuccess) {
+      rc = FLINT_MOE_ERR_CUDA;
+      continue;
+    }
+    for (auto& ge : kv.second.graphs)
+      if (cudaGraphExecDestroy(ge.exec) != cudaSuccess) rc = FLINT_MOE_ERR_CUDA;
+    kv.second.graphs.clear();
+  }
+  if (cur >= 0) cudaSetDevice(cur);
+  return rc;
+}
+
+int flint_moe_device_error(int reset) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != FLINT_MOE_OK) return st;
+  unsigned v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, ds->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (reset && cudaMemset(ds->err, 0, sizeof(unsigned)) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  return (int)(v & 0x7FFFFFFFu);
+}
+
+const char* flint_moe_status_string(int status) {
+  switch (status) {
+    case FLINT_MOE_OK: return "ok";
+    case FLINT_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case FLINT_MOE_ERR_UNSUPPORTED: return "unsupported shape, batch or format";
+    case FLINT_MOE_ERR_WORKSPACE: return "workspace or output buffer too small";
+    case FLINT_MOE_ERR_CUDA: return "CUDA runtime error";
+    case FLINT_MOE_ERR_TIMEOUT: return "a bounded device wait gave up";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,327 @@
+// Shared constants and sm_103a PTX helpers of the Flint MoE kernels.
+//
+// Packed expert layout (written by the packer, read by the decode kernels).
+// An expert is [64 gate/up tiles][128 down tiles].  A tile is 16 weight rows
+// cut into K-slices of 256 columns; one warp consumes one slice with 16
+// mma.m16n8k16 steps (one 16-column NVFP4 block per step).
+//   gate/up tile r: tile rows 0..7 = gate rows 8r..8r+7, rows 8..15 = up rows
+//     8r..8r+7, so the accumulator thread holding gate row j holds up row j
+//     too (SiLU*up needs no exchange); 8 slices cover K = 2048.
+//   down tile r: rows 16r..16r+15, 2 slices cover K = 512.
+// NVFP4 slice (2304 B): codes [4 chunks][32 lanes][16 B] + scales [2][8][16 B]
+//   lane L = 4g + t of chunk c holds, for the 4 blocks kb = 4c + j, the bytes
+//   {row g byte t, row g+8 byte t, row g byte t+4, row g+8 byte t+4} of block
+//   kb -- exactly the A-fragment registers {a0a1, a2a3, a4a5, a6a7} of one
+//   mma.m16n8k16 after an e2m1x2 -> f16x2 convert of each byte.
+//   scales: half h, group g: 8 blocks x (row g, row g+8) E4M3 bytes.
+// BF16 slice (8192 B): [16 blocks][32 lanes][16 B] A-fragment registers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace flint {
+
+constexpr int H = 2048;
+constexpr int E = 256;
+constexpr int NE = E + 1;  // routed + shared; expert E is the shared expert
+constexpr int I = 512;
+constexpr int TOPK = 6;
+constexpr int BMAX = 8;
+constexpr int MAX_SLOTS = 1 + BMAX * TOPK;  // shared + up to 48 unique routed
+
+constexpr int GU_TILES = 2 * I / 16;  // 64
+constexpr int DN_TILES = H / 16;      // 128
+constexpr int GU_SLICES = H / 256;    // 8
+constexpr int DN_SLICES = I / 256;    // 2
+
+constexpr int F4_SLICE = 2304;
+constexpr int F4_CODES = 2048;
+constexpr int F4_GU_TILE = GU_SLICES * F4_SLICE;  // 18432
+constexpr int F4_DN_TILE = DN_SLICES * F4_SLICE;  // 4608
+constexpr size_t F4_GU_BYTES = (size_t)GU_TILES * F4_GU_TILE;  // 1179648
+constexpr size_t F4_EXPERT = F4_GU_BYTES + (size_t)DN_TILES * F4_DN_TILE;  // 1769472
+
+constexpr int B16_SLICE = 8192;
+constexpr int B16_GU_TILE = GU_SLICES * B16_SLICE;  // 65536
+constexpr int B16_DN_TILE = DN_SLICES * B16_SLICE;  // 16384
+constexpr size_t B16_GU_BYTES = (size_t)GU_TILES * B16_GU_TILE;
+constexpr size_t B16_EXPERT = B16_GU_BYTES + (size_t)DN_TILES * B16_DN_TILE;  // 6291456
+
+// Error bits recorded in the device error word.
+constexpr unsigned ERR_WAIT_FULL = 1u;
+constexpr unsigned ERR_WAIT_EMPTY = 2u;
+constexpr unsigned ERR_DRAIN = 4u;
+
+// A bounded wait gives up after about one second at the maximum SM clock.
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete; false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+  }
+  return true;
+}
+
+// L2 policy for weights that are read once per step.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// One TMA bulk copy global -> shared, completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Four bytes of two E2M1 codes each -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2,
+                                                uint32_t& h3) {
+  asm("{\n .reg .b8 a0, a1, a2, a3;\n mov.b32 {a0, a1, a2, a3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, a0;\n cvt.rn.f16x2.e2m1x2 %1, a1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, a2;\n cvt.rn.f16x2.e2m1x2 %3, a3;\n}\n"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+// Two E4M3 bytes -> f16x2 (low byte -> low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_bytes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s) {
+  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), __low2half2(*reinterpret_cast<const __half2*>(&s)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
+  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), __high2half2(*reinterpret_cast<const __half2*>(&s)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ unsigned redux_max(unsigned v) {
+  unsigned r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ unsigned redux_min(unsigned v) {
+  unsigned r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+// ------------------------------------------------------- compensated summation
+// Knuth's TwoSum: s + e == a + b exactly.  Used where a rounding decision
+// (bf16 logits that feed top-k, the RMSNorm scale) must not depend on the
+// order of accumulation: products of bf16 values are exact in fp32, and the
+// compensated sum rounds to the same fp32 as the exact sum.
+struct CSum {
+  float s, c;
+};
+__device__ __forceinline__ void cs_add(CSum& x, float p) {
+  const float s = __fadd_rn(x.s, p);
+  const float z = __fsub_rn(s, x.s);
+  const float e = __fadd_rn(__fsub_rn(x.s, __fsub_rn(s, z)), __fsub_rn(p, z));
+  x.s = s;
+  x.c = __fadd_rn(x.c, e);
+}
+__device__ __forceinline__ void cs_merge(CSum& x, const CSum& y) {
+  cs_add(x, y.s);
+  x.c = __fadd_rn(x.c, y.c);
+}
+__device__ __forceinline__ CSum cs_warp_reduce(CSum x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    CSum y;
+    y.s = __shfl_xor_sync(0xffffffffu, x.s, off);
+    y.c = __shfl_xor_sync(0xffffffffu, x.c, off);
+    cs_merge(x, y);
+  }
+  return x;
+}
+__device__ __forceinline__ float cs_value(const CSum& x) { return __fadd_rn(x.s, x.c); }
+
+// ---------------------------------------------------------------- routing
+// Result of sigmoid top-6 for a batch, laid out for the expert kernels.
+// Slot 0 is the shared expert; slots 1..n_slots-1 are the distinct routed
+// experts chosen by any token, in ascending expert order.
+struct Routing {
+  int n_slots;
+  int slot_expert[MAX_SLOTS];
+  uint32_t slot_mask[MAX_SLOTS];  // bit t: token t uses the slot
+  float slot_w[MAX_SLOTS][BMAX];  // routing weight of token t (shared: 1)
+  int ids[BMAX][TOPK];
+  float w[BMAX][TOPK];
+  uint32_t umask[8];              // union of the selected experts, 256 bits
+  int ubase[8];                   // exclusive prefix of popc(umask)
+};
+
+// Computes the routing of B tokens from bf16 logits [B][256] (global memory,
+// written by the router kernel of the same sublayer).  Must be called by all
+// threads of a block of at least 8 warps; ends with __syncthreads.
+//   s = 1 / (1 + exp(-logit)) in fp32; top-6 by s, ties to the lower index;
+//   w_j = s_j / sum of the 6 selected s.
+__device__ __forceinline__ void compute_routing(const __nv_bfloat16* __restrict__ logits, int B, Routing& r) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < MAX_SLOTS * (BMAX + 2); i += blockDim.x) {
+    const int s = i / (BMAX + 2), k = i % (BMAX + 2);
+    if (k < BMAX) r.slot_w[s][k] = 0.f;
+    else if (k == BMAX) r.slot_mask[s] = 0u;
+    else r.slot_expert[s] = -1;
+  }
+  if (tid < 8) r.umask[tid] = 0u;
+  __syncthreads();
+  if (warp < B) {
+    const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(logits + (size_t)warp * E) + lane);
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t bits[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t hb = (wv[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
+      const float lg = __uint_as_float(hb << 16);
+      const float s = __frcp_rn(__fadd_rn(1.0f, expf(-lg)));
+      bits[i] = __float_as_uint(s);
+    }
+    uint32_t taken = 0u;
+    float sel_s[TOPK];
+    int sel_i[TOPK];
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) {
+      uint32_t best = 0u, bidx = 0xFFFFFFFFu;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (!((taken >> i) & 1u) && (bidx == 0xFFFFFFFFu || bits[i] > best)) {
+          best = bits[i];
+          bidx = lane * 8 + i;
+        }
+      }
+      const uint32_t m = redux_max(best);
+      const uint32_t win = redux_min(best == m ? bidx : 0xFFFFFFFFu);
+      if ((win >> 3) == (uint32_t)lane) taken |= 1u << (win & 7u);
+      sel_s[k] = __uint_as_float(m);
+      sel_i[k] = (int)win;
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) sum = __fadd_rn(sum, sel_s[k]);
+    if (lane < TOPK) {
+      float ws = 0.f;
+      int wi = 0;
+#pragma unroll
+      for (int k = 0; k < TOPK; ++k)
+        if (k == lane) {
+          ws = sel_s[k];
+          wi = sel_i[k];
+        }
+      r.ids[warp][lane] = wi;
+      r.w[warp][lane] = __fdiv_rn(ws, sum);
+      atomicOr(&r.umask[wi >> 5], 1u << (wi & 31));
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t m = lane < 8 ? r.umask[lane] : 0u;
+    const int cnt = __popc(m);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int base = incl - cnt;
+    if (lane < 8) {
+      r.ubase[lane] = base;
+      uint32_t mm = m;
+      int j = 0;
+      while (mm) {
+        const int b = __ffs(mm) - 1;
+        mm &= mm - 1;
+        r.slot_expert[1 + base + j] = lane * 32 + b;
+        ++j;
+      }
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 7);
+    if (lane == 0) {
+      r.n_slots = 1 + total;
+      r.slot_expert[0] = E;
+      r.slot_mask[0] = (B >= 32) ? 0xFFFFFFFFu : ((1u << B) - 1u);
+    }
+    if (lane < B) r.slot_w[0][lane] = 1.0f;
+  }
+  __syncthreads();
+  if (warp < B && lane < TOPK) {
+    const int e = r.ids[warp][lane];
+    const int wd = e >> 5;
+    const int slot = 1 + r.ubase[wd] + __popc(r.umask[wd] & ((1u << (e & 31)) - 1u));
+    r.slot_w[slot][warp] = r.w[warp][lane];
+    atomicOr(&r.slot_mask[slot], 1u << warp);
+  }
+  __syncthreads();
+}
+
+}  // namespace flint

@@ -111,7 +111,7 @@ def gen_layer(cfg: int, layer: int, device="cpu", weights: str | None = None,
     if weights == "nvfp4":
         def rbytes(name, shape, lo=0, hi=256):
             gg = _gen(s, layer, name, device)
-            return torch.randint(lo, hi, shape, generator=gg, device=device, dtype=torch.int32).to(torch.uint8)
+            return torch.randint(lo, hi, shape, generator=gg, device=device, dtype=torch.uint8)
         out["gu_codes"] = rbytes("gu_codes", (n, 2 * INTER, H // 2))
         out["gu_scales"] = rbytes("gu_scales", (n, 2 * INTER, H // BLOCK), SCALE_LO, SCALE_HI + 1)
         out["dn_codes"] = rbytes("dn_codes", (n, H, INTER // 2))

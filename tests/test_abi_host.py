@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a GPU (no compute call is made here)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_decode_router_gb300 import flint_moe as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flint_moe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return F.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flint_moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_calls_and_helpers():
+    names = declared_functions()
+    for n in ("flint_moe_pack_weights", "flint_moe_decode_layer", "flint_moe_decode_stack",
+              "flint_moe_prefill_layer", "flint_moe_packed_bytes", "flint_moe_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(declared_functions()) == set(F.EXPORTED)
+
+
+def test_packed_and_workspace_sizes(lib):
+    assert F.packed_bytes(F.W_NVFP4) == 257 * 1_769_472
+    assert F.packed_bytes(F.W_BF16) == 257 * 6_291_456
+    ws = F.workspace_bytes(F.W_NVFP4, 8)
+    assert ws > 0 and ws % 256 == 0
+    assert F.workspace_bytes(F.W_NVFP4, 1) == ws
+    bad = F.Dims(4096, 256, 1, 512, 6, 0, 1e-6)
+    assert lib.flint_moe_packed_bytes(ctypes.byref(bad)) == 0
+    assert lib.flint_moe_workspace_bytes(ctypes.byref(bad), 8) == 0
+
+
+FAKE = 0x7f0000000000  # 256-aligned address never dereferenced: validation fails first
+
+
+def _layer(**kw):
+    base = dict(router_w=FAKE, experts=FAKE + 256, tensor_scales=FAKE + 512, norm_w=None)
+    base.update(kw)
+    return F.Layer(base["router_w"], base["experts"], base["tensor_scales"], base["norm_w"])
+
+
+def _decode(lib, d=None, L=None, x=FAKE + 1024, B=1, y=FAKE + 2048, ws=FAKE + 4096, ws_bytes=None):
+    d = d or F.dims()
+    L = L or _layer()
+    ws_bytes = F.workspace_bytes() if ws_bytes is None else ws_bytes
+    return lib.flint_moe_decode_layer(ctypes.byref(d), ctypes.byref(L), x, B, y, None, None, ws, ws_bytes, None)
+
+
+def test_decode_rejects_bad_arguments_on_host(lib):
+    assert _decode(lib, B=9) == F.FLINT_MOE_ERR_UNSUPPORTED        # beyond the low-latency cap
+    assert _decode(lib, B=0) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert _decode(lib, x=None) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert _decode(lib, x=FAKE + 1032) == F.FLINT_MOE_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _decode(lib, y=FAKE + 1024) == F.FLINT_MOE_ERR_INVALID_ARG  # y aliases x
+    assert _decode(lib, ws=FAKE + 4112) == F.FLINT_MOE_ERR_INVALID_ARG  # ws not 256-byte aligned
+    assert _decode(lib, ws_bytes=1024) == F.FLINT_MOE_ERR_WORKSPACE
+    assert _decode(lib, L=_layer(router_w=None)) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert _decode(lib, L=_layer(tensor_scales=None)) == F.FLINT_MOE_ERR_INVALID_ARG  # NVFP4 needs scales
+    assert _decode(lib, d=F.Dims(2048, 128, 1, 512, 6, 0, 1e-6)) == F.FLINT_MOE_ERR_UNSUPPORTED
+    assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 8, 0, 1e-6)) == F.FLINT_MOE_ERR_UNSUPPORTED
+    assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 6, 7, 1e-6)) == F.FLINT_MOE_ERR_UNSUPPORTED
+    assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 6, 0, float("nan"))) == F.FLINT_MOE_ERR_INVALID_ARG
+
+
+def test_stack_and_pack_reject_bad_arguments_on_host(lib):
+    d = F.dims()
+    arr = (F.Layer * 2)(_layer(), _layer(router_w=None))
+    ws_b = F.workspace_bytes()
+    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 2, FAKE + 1024, 1, FAKE + 2048, None, None, None,
+                                    FAKE + 4096, ws_b, None)
+    assert rc == F.FLINT_MOE_ERR_INVALID_ARG
+    arr = (F.Layer * 1)(_layer())
+    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 0, FAKE + 1024, 1, FAKE + 2048, None, None, None,
+                                    FAKE + 4096, ws_b, None)
+    assert rc == F.FLINT_MOE_ERR_INVALID_ARG
+    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 1, FAKE + 1024, 12, FAKE + 2048, None, None, None,
+                                    FAKE + 4096, ws_b, None)
+    assert rc == F.FLINT_MOE_ERR_UNSUPPORTED
+    # NVFP4 pack needs both scale tensors; BF16 pack must not get any
+    rc = lib.flint_moe_pack_weights(ctypes.byref(d), FAKE, None, FAKE + 256, FAKE + 512, FAKE + 1024,
+                                    F.packed_bytes(), None)
+    assert rc == F.FLINT_MOE_ERR_INVALID_ARG
+    db = F.dims(F.W_BF16)
+    rc = lib.flint_moe_pack_weights(ctypes.byref(db), FAKE, FAKE + 16, FAKE + 256, None, FAKE + 1024,
+                                    F.packed_bytes(F.W_BF16), None)
+    assert rc == F.FLINT_MOE_ERR_INVALID_ARG
+    rc = lib.flint_moe_pack_weights(ctypes.byref(d), FAKE, FAKE + 16, FAKE + 256, FAKE + 512, FAKE + 1024,
+                                    100, None)
+    assert rc == F.FLINT_MOE_ERR_WORKSPACE
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert lib.flint_moe_status_string(st)
+    assert lib.flint_moe_status_string(-99) == b"unknown status"
