@@ -52,8 +52,10 @@ METRIC = "MoE decode µs/layer & effective HBM GB/s (% of roofline) at batch 1 a
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=N_LAYERS,
+                    help="sublayers in the stack (47 for the benchmark; fewer only for profiling captures)")
     ap.add_argument("--workload", default="stack47_b1_nvfp4", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -164,11 +166,11 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_stack(F, synth, torch, wl, dev):
+def build_stack(F, synth, torch, wl, dev, n_layers):
     fmt = wl["fmt"]
     cfg = 1 if fmt == "nvfp4" else 3  # the NVFP4 stacks share one weight set (config-1 seeds)
     layers = []
-    for i in range(N_LAYERS):
+    for i in range(n_layers):
         p = synth.gen_layer(cfg, i, device=dev)
         L = F.pack_layer(p, device=dev)
         torch.cuda.synchronize()
@@ -195,21 +197,22 @@ def run_ours(args):
     wl = WORKLOADS[args.workload]
     B = wl["batch"]
     fmt = F.W_NVFP4 if wl["fmt"] == "nvfp4" else F.W_BF16
-    layers = build_stack(F, synth, torch, wl, dev)
+    NL = args.layers
+    layers = build_stack(F, synth, torch, wl, dev, NL)
     xs = [synth.gen_x(wl["cfg"], B, index=i, device=dev) for i in range(N_INPUTS)]
     ys = [torch.empty_like(x) for x in xs]
     ws = F.alloc_workspace(fmt, B, device=dev)
 
     # Algorithmic bytes per input: router + (distinct routed + shared) experts per sublayer.
     expert_bytes = NVFP4_EXPERT_BYTES if fmt == F.W_NVFP4 else BF16_EXPERT_BYTES
-    ids = torch.empty((N_LAYERS, B, 6), dtype=torch.int32, device=dev)
+    ids = torch.empty((NL, B, 6), dtype=torch.int32, device=dev)
     bytes_per_input = []
     uniq = []
     for i, x in enumerate(xs):
         F.decode_stack(layers, x, ys[i], ws, ids_per_layer=ids)
         torch.cuda.synchronize()
         idc = ids.cpu()
-        u = [len(set(idc[l].flatten().tolist())) for l in range(N_LAYERS)]
+        u = [len(set(idc[l].flatten().tolist())) for l in range(NL)]
         uniq.extend(u)
         bytes_per_input.append(sum(ROUTER_BYTES + (n + 1) * expert_bytes for n in u))
     # Prime one cached graph per input buffer (the graph bakes in pointers).
@@ -269,7 +272,7 @@ def run_ours(args):
         tdist.all_reduce(ms_t, op=tdist.ReduceOp.MAX)
     ms = float(ms_t.item())
     ms_per_step = ms / args.steps
-    us_per_layer = ms_per_step * 1000.0 / N_LAYERS
+    us_per_layer = ms_per_step * 1000.0 / NL
     total_bytes = sum(bytes_per_input[s % N_INPUTS] for s in range(args.steps))
     gbs = total_bytes / (ms / 1000.0) / 1e9
     peaks = {}
@@ -279,7 +282,7 @@ def run_ours(args):
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    bytes_per_layer = total_bytes / args.steps / N_LAYERS
+    bytes_per_layer = total_bytes / args.steps / NL
     out = {
         "metric": METRIC,
         "value": round(us_per_layer, 3),
@@ -294,7 +297,7 @@ def run_ours(args):
         "dtype": "nvfp4-w/bf16-a (f32 accumulate)" if fmt == F.W_NVFP4 else "bf16 (f32 accumulate)",
         "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
         "config": {
-            "workload": args.workload, "layers": N_LAYERS, "batch": B, "hidden": 2048, "experts": "256+1",
+            "workload": args.workload, "layers": NL, "batch": B, "hidden": 2048, "experts": "256+1",
             "inter": 512, "top_k": 6, "weights": wl["fmt"], "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2: 16 rotating batches, >=631 MB touched per step, weights resident "
                   f"{len(layers) * F.packed_bytes(fmt) / 1e9:.1f} GB",
@@ -307,9 +310,9 @@ def run_ours(args):
             "frac": round(gbs / peak, 4), "peak_source": peak_src,
             "bytes_per_layer": round(bytes_per_layer), "traffic": None,
         },
-        "e2e": {"value": round(e2e_ms * 1000.0 / N_LAYERS, 3), "unit": "us/layer",
+        "e2e": {"value": round(e2e_ms * 1000.0 / NL, 3), "unit": "us/layer",
                 "h2d_bytes_per_step": B * 2048 * 2, "d2h_bytes_per_step": B * 2048 * 2},
-        "gpu_launches": args.steps * N_LAYERS * 3,
+        "gpu_launches": args.steps * NL * 3,
         "clocks": clk,
         "device_error_word": err,
     }

@@ -102,6 +102,11 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 
 // ------------------------------------------------------------------ router
 
+// x_hat in mma B-fragment order: [8 K-slices][32 lanes][16 blocks][2 regs]
+// (u32 each, two 16-bit values), lane = 4 * token + t.  A consumer warp of
+// slice w loads its 16 blocks' fragments with eight 16-byte loads.
+constexpr int XFRAG_WORDS = 8 * 32 * 16 * 2;
+
 struct RouterParams {
   const __nv_bfloat16* x;       // [B][H]
   const CSum* ss_in;            // [DN_TILES][8] sum-of-squares partials of x, or null
@@ -110,23 +115,24 @@ struct RouterParams {
   float eps;
   int want_f16;
   __nv_bfloat16* logits;   // [B][E]
-  __nv_bfloat16* xh_bf16;  // [B][H]
-  __half* xh_f16;          // [B][H]
+  __nv_bfloat16* xh_bf16;  // [B][H] natural layout
+  uint32_t* xfrag_f16;     // x_hat * 2^xh_exp[token] in f16, fragment order
+  uint32_t* xfrag_bf16;    // x_hat in bf16, fragment order
   int* xh_exp;             // [B]
 };
 
 // Router logits logit[t][e] = bf16( sum_k x_hat[t][k] * W_r[e][k] ).  The sum
-// is accumulated error-free (products of bf16 values are exact in fp32) so
-// the bf16 logit, which decides the top-6, is the correctly rounded value and
-// does not depend on the order of accumulation.  Each CTA owns EPC experts;
-// thread k owns columns [8k, 8k+8).
-template <int EPC, int NB>
-__global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
-  constexpr int V = EPC * NB;
-  constexpr int VP = Pow2Ceil<V>::value;
-  constexpr int NBP = Pow2Ceil<NB>::value;
+// is accumulated error-free (products of bf16 values are exact in fp32;
+// TwoSum carries the rounding error), so the bf16 logit that decides the top-6
+// is the correctly rounded value whatever the order of accumulation.  CTA e
+// owns expert e; thread k owns columns [8k, 8k+8); token pairs share packed
+// fp32x2 arithmetic.
+template <int NB, int EPC>
+__global__ void __launch_bounds__(256, 2) router_kernel(const RouterParams p) {
+  constexpr int NP = (NB + 1) / 2;
+  constexpr int VP = Pow2Ceil<NB * EPC>::value;
+  constexpr int SH = 5 - Log2<VP>::value;
   __shared__ CSum red[8][VP];
-  __shared__ CSum ssred[8][NBP];
   __shared__ float rscale[NB];
   __shared__ unsigned xmax[NB];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -146,17 +152,37 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
   pdl_trigger();
   pdl_wait();
 
-  float xv[NB][8];
+  // Issue every dependent load before using any of them (one round trip).
+  uint4 xraw[NB];
 #pragma unroll
-  for (int t = 0; t < NB; ++t)
-    bf16x8_to_f32(__ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H + k0)), xv[t]);
+  for (int t = 0; t < NB; ++t) xraw[t] = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H + k0));
+  const bool ss_given = has_norm && p.ss_in != nullptr;
+  CSum ssp[DN_TILES / 32];
+  if (ss_given && warp < NB) {
+#pragma unroll
+    for (int j = 0; j < DN_TILES / 32; ++j) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(p.ss_in + (lane + 32 * j) * BMAX + warp));
+      ssp[j] = CSum{v.x, v.y};
+    }
+  }
+  float xv[2 * NP][8];
+#pragma unroll
+  for (int t = 0; t < 2 * NP; ++t) {
+    if (t < NB) {
+      bf16x8_to_f32(xraw[t], xv[t]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xv[t][i] = 0.f;
+    }
+  }
 
   if (has_norm) {
-    if (p.ss_in != nullptr) {
+    if (ss_given) {
       // Partials written by the previous sublayer's down kernel.
       if (warp < NB) {
-        CSum a = {0.f, 0.f};
-        for (int j = lane; j < DN_TILES; j += 32) cs_merge(a, p.ss_in[j * BMAX + warp]);
+        CSum a = ssp[0];
+#pragma unroll
+        for (int j = 1; j < DN_TILES / 32; ++j) cs_merge(a, ssp[j]);
         a = cs_warp_reduce(a);
         if (lane == 0) {
           const float ms = __fmul_rn(cs_value(a), 1.0f / (float)H);
@@ -164,21 +190,35 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
         }
       }
     } else {
-      CSum ss[NBP];
+      CSum2 ss2[NP];
 #pragma unroll
-      for (int t = 0; t < NBP; ++t) ss[t] = CSum{0.f, 0.f};
+      for (int q = 0; q < NP; ++q) ss2[q] = CSum2{0ull, 0ull};
 #pragma unroll
-      for (int t = 0; t < NB; ++t)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cs_add(ss[t], __fmul_rn(xv[t][i], xv[t][i]));
-      const CSum tot = cs_reduce_scatter<NBP>(ss, lane);
-      constexpr int SH = 5 - Log2<NBP>::value;
-      if ((lane & ((1 << SH) - 1)) == 0) ssred[warp][lane >> SH] = tot;
+        for (int q = 0; q < NP; ++q) {
+          const uint64_t v = f2pack(xv[2 * q][i], xv[2 * q + 1][i]);
+          cs2_add(ss2[q], f2mul(v, v));
+        }
+      constexpr int VN = Pow2Ceil<NB>::value;
+      constexpr int SHN = 5 - Log2<VN>::value;
+      CSum ss[VN];
+#pragma unroll
+      for (int v = 0; v < VN; ++v) ss[v] = CSum{0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        CSum lo, hi;
+        cs2_split(ss2[q], lo, hi);
+        ss[2 * q] = lo;
+        if (2 * q + 1 < VN) ss[2 * q + 1] = hi;
+      }
+      const CSum tot = cs_reduce_scatter<VN>(ss, lane);
+      if ((lane & ((1 << SHN) - 1)) == 0) red[warp][lane >> SHN] = tot;
       __syncthreads();
       if (tid < NB) {
-        CSum a = ssred[0][tid];
+        CSum a = red[0][tid];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) cs_merge(a, ssred[w][tid]);
+        for (int w = 1; w < 8; ++w) cs_merge(a, red[w][tid]);
         const float ms = __fmul_rn(cs_value(a), 1.0f / (float)H);
         rscale[tid] = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, p.eps)));
       }
@@ -193,31 +233,51 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
     }
   }
 
-  CSum d[VP];
-#pragma unroll
-  for (int v = 0; v < VP; ++v) d[v] = CSum{0.f, 0.f};
+  CSum2 d2[EPC][NP];
 #pragma unroll
   for (int j = 0; j < EPC; ++j)
 #pragma unroll
-    for (int t = 0; t < NB; ++t)
+    for (int q = 0; q < NP; ++q) d2[j][q] = CSum2{0ull, 0ull};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) cs_add(d[j * NB + t], __fmul_rn(xv[t][i], wf[j][i]));
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int j = 0; j < EPC; ++j) {
+      const uint64_t w2 = f2pack(wf[j][i], wf[j][i]);
+#pragma unroll
+      for (int q = 0; q < NP; ++q) cs2_add(d2[j][q], f2mul(f2pack(xv[2 * q][i], xv[2 * q + 1][i]), w2));
+    }
+  }
   {
+    // value v = j * NB + t (expert e0 + j, token t)
+    CSum d[VP];
+#pragma unroll
+    for (int v = 0; v < VP; ++v) d[v] = CSum{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < EPC; ++j)
+#pragma unroll
+      for (int q = 0; q < NP; ++q) {
+        CSum lo, hi;
+        cs2_split(d2[j][q], lo, hi);
+        d[j * NB + 2 * q] = lo;
+        if (2 * q + 1 < NB) d[j * NB + 2 * q + 1] = hi;
+      }
     const CSum tot = cs_reduce_scatter<VP>(d, lane);
-    constexpr int SH = 5 - Log2<VP>::value;
+    __syncthreads();  // red may still hold the norm partials
     if ((lane & ((1 << SH) - 1)) == 0) red[warp][lane >> SH] = tot;
   }
   __syncthreads();
-  if (tid < V) {
+  if (tid < NB * EPC) {
     CSum a = red[0][tid];
 #pragma unroll
     for (int w = 1; w < 8; ++w) cs_merge(a, red[w][tid]);
-    const int j = tid / NB, t = tid % NB;
-    p.logits[(size_t)t * E + e0 + j] = __float2bfloat16_rn(cs_value(a));
+    p.logits[(size_t)(tid % NB) * E + e0 + tid / NB] = __float2bfloat16_rn(cs_value(a));
   }
 
   if (blockIdx.x == 0) {
-    // Every CTA computed the same x_hat; CTA 0 publishes it.
+    // Every CTA computed the same x_hat; CTA 0 publishes it, natural and in
+    // fragment order.  Columns 8k..8k+7 are block kb = (k % 32) / 2, register
+    // r = k % 2 of K-slice k / 32, lanes 4t..4t+3 of token t.
+    const int ws = k0 >> 8, kb = (k0 & 255) >> 4, rr = (k0 >> 3) & 1;
 #pragma unroll
     for (int t = 0; t < NB; ++t) {
       uint32_t pk[4];
@@ -225,6 +285,8 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
       for (int i = 0; i < 4; ++i)
         pk[i] = (__float_as_uint(xv[t][2 * i]) >> 16) | (__float_as_uint(xv[t][2 * i + 1]) & 0xFFFF0000u);
       *reinterpret_cast<uint4*>(p.xh_bf16 + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p.xfrag_bf16[((ws * 32 + 4 * t + i) * 16 + kb) * 2 + rr] = pk[i];
     }
     if (p.want_f16) {
 #pragma unroll
@@ -240,13 +302,11 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
       for (int t = 0; t < NB; ++t) {
         const int ex = f16_range_exp(__uint_as_float(xmax[t]));
         const float sc = exp2i(ex);
-        uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const __half2 hv = __floats2half2_rn(__fmul_rn(xv[t][2 * i], sc), __fmul_rn(xv[t][2 * i + 1], sc));
-          pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+          p.xfrag_f16[((ws * 32 + 4 * t + i) * 16 + kb) * 2 + rr] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        *reinterpret_cast<uint4*>(p.xh_f16 + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         if (tid == 0) p.xh_exp[t] = ex;
       }
     }
@@ -255,14 +315,20 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterParams p) {
 
 // ------------------------------------------------------------------ expert GEMV slices
 
-// 16 weight rows x 256 columns of NVFP4 (one packed slice in shared memory)
-// times 256 x 8 activations (B fragments in registers), fp32 accumulate.
+// 16 weight rows x 256 columns (one packed slice in shared memory) times
+// 256 x 8 activations (B fragments in registers), fp32 accumulate.  Four
+// independent accumulator chains keep the tensor pipe busy.
 __device__ __forceinline__ void nvfp4_slice_mma(const uint8_t* sl, int lane, const uint32_t (&bfr)[16][2],
                                                 float (&acc)[4]) {
   const int g = lane >> 2;
   const uint4 s0 = *reinterpret_cast<const uint4*>(sl + F4_CODES + g * 16);
   const uint4 s1 = *reinterpret_cast<const uint4*>(sl + F4_CODES + 128 + g * 16);
   const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  float a4[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a4[c][j] = 0.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint4 cw = *reinterpret_cast<const uint4*>(sl + c * 512 + lane * 16);
@@ -277,18 +343,27 @@ __device__ __forceinline__ void nvfp4_slice_mma(const uint8_t* sl, int lane, con
       a1 = hmul2_hi(a1, sc);
       a2 = hmul2_lo(a2, sc);
       a3 = hmul2_hi(a3, sc);
-      mma_f16(acc, a0, a1, a2, a3, bfr[kb][0], bfr[kb][1]);
+      mma_f16(a4[j], a0, a1, a2, a3, bfr[kb][0], bfr[kb][1]);
     }
   }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
 }
 
 __device__ __forceinline__ void bf16_slice_mma(const uint8_t* sl, int lane, const uint32_t (&bfr)[16][2],
                                                float (&acc)[4]) {
+  float a4[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a4[c][j] = 0.f;
 #pragma unroll
   for (int kb = 0; kb < 16; ++kb) {
     const uint4 a = *reinterpret_cast<const uint4*>(sl + kb * 512 + lane * 16);
-    mma_bf16(acc, a.x, a.y, a.z, a.w, bfr[kb][0], bfr[kb][1]);
+    mma_bf16(a4[kb & 3], a.x, a.y, a.z, a.w, bfr[kb][0], bfr[kb][1]);
   }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
 }
 
 template <int FMT>
@@ -316,19 +391,25 @@ struct Fmt<1> {
   }
 };
 
-// ------------------------------------------------------------------ gate/up
 static_assert(sizeof(Routing) % 4 == 0, "Routing must keep 4-byte alignment");
 static_assert(F4_GU_TILE % 128 == 0 && F4_DN_TILE % 128 == 0 && B16_GU_TILE % 128 == 0 &&
                   B16_DN_TILE % 128 == 0,
               "stage buffers must keep 16-byte (bulk copy) alignment");
 static_assert(F4_SLICE % 16 == 0 && B16_SLICE % 16 == 0, "slices are read with 16-byte loads");
 
+// Partial accumulators of one item, one warp: [4 registers][32 lanes] fp32.
+// Register j of lane 4g+t holds row g (j < 2) or g + 8 (j >= 2), token 2t + (j & 1).
+__device__ __forceinline__ int red_off(int row, int tk) {
+  return ((row >> 3) * 2 + (tk & 1)) * 32 + 4 * (row & 7) + (tk >> 1);
+}
+
+// ------------------------------------------------------------------ gate/up
 
 struct GateUpParams {
   const uint8_t* experts;
   const float* tscale;          // [NE][2] (NVFP4)
   const __nv_bfloat16* logits;  // [B][E]
-  const void* xh;               // f16 [B][H] (NVFP4) or bf16 [B][H]
+  const uint32_t* xfrag;        // x_hat B fragments: f16 (NVFP4) or bf16
   const int* xh_exp;            // [B] (NVFP4)
   int B;
   __nv_bfloat16* h;             // [MAX_SLOTS][BMAX][I]
@@ -338,42 +419,64 @@ struct GateUpParams {
   unsigned* err;
 };
 
-constexpr int GU_THREADS = 288;  // 8 consumer warps (one K slice each) + 1 producer warp
+// 8 compute warps (one K slice each), 1 TMA producer warp, 2 epilogue warps.
+constexpr int GU_COMPUTE_WARPS = 8;
+constexpr int GU_PRODUCER_WARP = 8;
+constexpr int GU_THREADS = 32 * (GU_COMPUTE_WARPS + 1 + 2);  // 352
+constexpr int GU_RED = 4;  // depth of the partial-sum ring between compute and epilogue warps
+constexpr int TSCALE_WORDS = ((NE * 2 + 3) / 4) * 4;  // per-expert (gate/up, down) scales, padded
 
 template <int FMT, int STAGES>
 __host__ __device__ constexpr size_t gateup_smem_bytes() {
-  // [stages][red 2x8x128 fp32][full, empty barriers][abort flag, pad to 16][Routing]
-  return (size_t)STAGES * Fmt<FMT>::GU_TILE + 2 * 8 * 128 * 4 + 2 * STAGES * 8 + 16 + sizeof(Routing);
+  // [stages][red ring GU_RED x 8 x 128 fp32][tensor scales][full, empty][rfull, rempty][pad 16][Routing]
+  return (size_t)STAGES * Fmt<FMT>::GU_TILE + GU_RED * 8 * 128 * 4 + TSCALE_WORDS * 4 + 2 * STAGES * 8 +
+         2 * GU_RED * 8 + 16 + sizeof(Routing);
 }
 
+// Items are (slot, row tile) pairs, item i = slot * 64 + tile; CTA b takes
+// items b, b + G, b + 2G, ...  One item is one 18 KiB (NVFP4) bulk copy.  The
+// 8 compute warps each multiply one K-slice of it and pass their partial sums
+// through a ring of GU_RED buffers to the 2 epilogue warps, which reduce them
+// in a fixed order and apply SiLU*up.  Compute warps never wait on the
+// epilogue unless the ring is full.
 template <int FMT, int STAGES>
 __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParams p) {
   using F = Fmt<FMT>;
   constexpr int TILE = F::GU_TILE;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)STAGES * TILE);  // [2][8][128], 16-byte aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 2 * 8 * 128);
+  float* red = reinterpret_cast<float*>(smem + (size_t)STAGES * TILE);  // [GU_RED][8][128], 16-byte aligned
+  float* ts_s = red + GU_RED * 8 * 128;                                   // [NE][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ts_s + TSCALE_WORDS);
   uint64_t* empty = full + STAGES;
-  int* abort_flag = reinterpret_cast<int*>(empty + STAGES);
-  Routing& R = *reinterpret_cast<Routing*>(reinterpret_cast<uint8_t*>(abort_flag) + 16);
+  uint64_t* rfull = empty + STAGES;
+  uint64_t* rempty = rfull + GU_RED;
+  Routing& R = *reinterpret_cast<Routing*>(reinterpret_cast<uint8_t*>(rempty + GU_RED) + 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, bid = blockIdx.x;
+  const int B = p.B;
+  if (FMT == 0)
+    for (int q = tid; q < NE * 2; q += GU_THREADS) ts_s[q] = __ldg(p.tscale + q);  // constants
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 8);
+      mbar_init(&empty[s], GU_COMPUTE_WARPS);
     }
-    *abort_flag = 0;
+#pragma unroll
+    for (int b = 0; b < GU_RED; ++b) {
+      mbar_init(&rfull[b], GU_COMPUTE_WARPS);
+      mbar_init(&rempty[b], 2);
+    }
     fence_mbar_init();
   }
+  zero_routing(R, tid, GU_THREADS);
   __syncthreads();
 
   const uint64_t pol = l2_evict_first();
   int issued = 0;
-  if (tid == 256) {
+  if (tid == GU_PRODUCER_WARP * 32) {
     // The shared expert's tiles do not depend on the routing: request them
     // while the router is still running.
     for (; issued < STAGES; ++issued) {
@@ -386,15 +489,44 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   }
 
   pdl_wait();
-  compute_routing(p.logits, p.B, R);
+  const int g = lane >> 2;
+  // The routing input first: the top-k waits on it, the B fragments are needed later.
+  uint4 lraw = make_uint4(0u, 0u, 0u, 0u);
+  if (warp < B) lraw = load_logits(p.logits + (size_t)warp * E, lane);
+  uint32_t bfr[16][2];
+  if (warp < GU_COMPUTE_WARPS) {
+    if (g < B) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.xfrag + (size_t)(warp * 32 + lane) * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = __ldcg(src + q);
+        bfr[2 * q][0] = v.x;
+        bfr[2 * q][1] = v.y;
+        bfr[2 * q + 1][0] = v.z;
+        bfr[2 * q + 1][1] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < 16; ++kb) bfr[kb][0] = bfr[kb][1] = 0u;
+    }
+  }
+  if (warp < B) warp_topk(lraw, lane, R.ids[warp], R.w[warp], R.umask);
+  __syncthreads();
   pdl_trigger();  // the down kernel may start: the routing inputs are final
-  const int n_items = R.n_slots * GU_TILES;
-  if (bid == 0 && tid < p.B * TOPK) {
+  int n_slots = 1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) n_slots += __popc(R.umask[i]);
+  const int n_items = n_slots * GU_TILES;
+  if (bid == 0 && tid < B * TOPK) {
     if (p.ids_out) p.ids_out[tid] = R.ids[tid / TOPK][tid % TOPK];
     if (p.w_out) p.w_out[tid] = R.w[tid / TOPK][tid % TOPK];
   }
 
-  if (warp == 8) {
+  if (warp == GU_PRODUCER_WARP) {
+    // The slot table is written before any routed tile is requested; a reader
+    // of it first waits on such a tile's barrier (or on a partial-sum barrier
+    // downstream of one), which orders the table writes before its reads.
+    warp_slot_table(R, B, lane);
     if (lane == 0) {
       for (int n = issued;; ++n) {
         const int i = bid + n * G;
@@ -419,88 +551,72 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
     return;
   }
 
-  // ---- consumers: warp w multiplies K slice w of every tile
-  const int g = lane >> 2, t = lane & 3;
-  uint32_t bfr[16][2];
-  if (g < p.B) {
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(p.xh) + (size_t)g * H +
-                                                           warp * 256);
+  if (warp < GU_COMPUTE_WARPS) {
+    // ---- compute warps: warp w multiplies K slice w of every tile
+    for (int n = 0;; ++n) {
+      const int i = bid + n * G;
+      if (i >= n_items) break;
+      const int s = n % STAGES;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mbar_wait(&full[s], (n / STAGES) & 1)) {
+        F::slice(stages + (size_t)s * TILE + warp * F::SLICE, lane, bfr, acc);
+      } else {
+        atomicOr(p.err, ERR_WAIT_FULL);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      const int b = n % GU_RED;
+      if (n >= GU_RED && !mbar_wait(&rempty[b], ((n / GU_RED) - 1) & 1)) atomicOr(p.err, ERR_WAIT_EMPTY);
+      float* rb = red + b * 1024;
 #pragma unroll
-    for (int kb = 0; kb < 16; ++kb) {
-      bfr[kb][0] = __ldcg(xr + kb * 8 + t);
-      bfr[kb][1] = __ldcg(xr + kb * 8 + t + 4);
+      for (int j = 0; j < 4; ++j) rb[warp * 128 + j * 32 + lane] = acc[j];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[b]);
     }
-  } else {
-#pragma unroll
-    for (int kb = 0; kb < 16; ++kb) bfr[kb][0] = bfr[kb][1] = 0u;
+    return;
   }
-  float xs[2] = {1.f, 1.f};  // 2^-exponent of tokens 2t, 2t+1 (NVFP4)
-  if (FMT == 0) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (2 * t + q < p.B) xs[q] = exp2i(-__ldcg(p.xh_exp + 2 * t + q));
-  }
-  float hm[2] = {0.f, 0.f};
 
+  // ---- epilogue warps: thread = (token ep_tk, gate/up row ep_row of the tile)
+  const int et = tid - (GU_PRODUCER_WARP + 1) * 32;
+  const int ep_tk = et >> 3, ep_row = et & 7;
+  float xs = 1.f;  // 2^-exponent of token ep_tk (NVFP4)
+  if (FMT == 0 && ep_tk < B) xs = exp2i(-__ldcg(p.xh_exp + ep_tk));
+  float hm = 0.f;
+  const int og = red_off(ep_row, ep_tk), ou = red_off(ep_row + 8, ep_tk);
   for (int n = 0;; ++n) {
     const int i = bid + n * G;
     if (i >= n_items) break;
-    const int s = n % STAGES;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mbar_wait(&full[s], (n / STAGES) & 1)) {
-      F::slice(stages + (size_t)s * TILE + warp * F::SLICE, lane, bfr, acc);
-    } else {
+    const int b = n % GU_RED;
+    if (!mbar_wait(&rfull[b], (n / GU_RED) & 1)) {
       atomicOr(p.err, ERR_WAIT_FULL);
-      *abort_flag = 1;
+      break;
+    }
+    const float* rb = red + b * 1024;
+    const int slot = i / GU_TILES, tile = i % GU_TILES;
+    const uint32_t mask = slot == 0 ? ((1u << B) - 1u) : R.slot_mask[slot];
+    if (ep_tk < B && ((mask >> ep_tk) & 1u)) {
+      const int e = slot == 0 ? E : R.slot_expert[slot];
+      float gsum = 0.f, usum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        gsum += rb[w * 128 + og];
+        usum += rb[w * 128 + ou];
+      }
+      const float f = FMT == 0 ? __fmul_rn(xs, ts_s[2 * e]) : 1.0f;
+      const float gate = __fmul_rn(gsum, f);
+      const float up = __fmul_rn(usum, f);
+      const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
+      const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
+      p.h[((size_t)slot * BMAX + ep_tk) * I + tile * 8 + ep_row] = hv;
+      hm = fmaxf(hm, fabsf(__bfloat162float(hv)));
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    float* rb = red + (n & 1) * 1024;
-    *reinterpret_cast<float4*>(rb + warp * 128 + lane * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    named_bar_sync(1, 256);
-    if (*abort_flag) break;
-    if (warp == 0) {
-      float c[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = rb[lane * 4 + j];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) {
-        const float4 v = *reinterpret_cast<const float4*>(rb + w * 128 + lane * 4);
-        c[0] += v.x;
-        c[1] += v.y;
-        c[2] += v.z;
-        c[3] += v.w;
-      }
-      const int slot = i / GU_TILES, tile = i % GU_TILES;
-      const int e = R.slot_expert[slot];
-      const uint32_t mask = R.slot_mask[slot];
-      const float ts = FMT == 0 ? __ldg(p.tscale + 2 * e) : 1.0f;
-      const int j = tile * 8 + g;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int tk = 2 * t + q;
-        if ((mask >> tk) & 1u) {
-          const float f = __fmul_rn(xs[q], ts);
-          const float gate = __fmul_rn(c[q], f);
-          const float up = __fmul_rn(c[2 + q], f);
-          const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
-          const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
-          p.h[((size_t)slot * BMAX + tk) * I + j] = hv;
-          hm[q] = fmaxf(hm[q], fabsf(__bfloat162float(hv)));
-        }
-      }
-    }
+    if (lane == 0) mbar_arrive(&rempty[b]);
   }
-  if (warp == 0) {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      float m = hm[q];
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      if (g == 0) p.hmax_part[(size_t)bid * BMAX + 2 * t + q] = m;
-    }
-  }
+  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 1));
+  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 2));
+  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 4));
+  if (ep_row == 0) p.hmax_part[(size_t)bid * BMAX + ep_tk] = hm;
 }
 
 // ------------------------------------------------------------------ down + combine
@@ -519,47 +635,63 @@ struct DownParams {
   unsigned* err;
 };
 
-constexpr int DN_THREADS = 288;
 constexpr int HS_STRIDE = 520;  // halves per staged h row: 512 + 8 so rows land 4 banks apart
+constexpr int MAX_HPARTS = 512;
 
-template <int FMT, int STAGES>
+template <int NG>
+struct DnCfg {
+  static constexpr int COMPUTE_WARPS = 2 * NG;  // NG slot groups x 2 K halves
+  static constexpr int THREADS = 32 * (COMPUTE_WARPS + 1);
+};
+
+template <int FMT, int STAGES, int NG>
 __host__ __device__ constexpr size_t down_smem_fixed() {
-  // [stages][red 8x128 fp32][full, empty barriers][hexp 8, misc 8 ints][pidx][pair token][pair slot][Routing]
-  return (size_t)STAGES * Fmt<FMT>::DN_TILE + 8 * 128 * 4 + 2 * STAGES * 8 + 64 + MAX_SLOTS * BMAX + 64 + 64 +
-         sizeof(Routing);
+  // [stages][red (2NG) x 128 fp32][tensor scales][full, empty barriers][hexp 8, misc 8 ints][pidx]
+  // [pair token][pair slot][Routing]
+  return (size_t)STAGES * Fmt<FMT>::DN_TILE + DnCfg<NG>::COMPUTE_WARPS * 128 * 4 + TSCALE_WORDS * 4 +
+         2 * STAGES * 8 + 64 + MAX_SLOTS * BMAX + 64 + 64 + sizeof(Routing);
 }
-template <int FMT, int STAGES>
+template <int FMT, int STAGES, int NG>
 size_t down_smem_bytes(int B) {
-  return ((down_smem_fixed<FMT, STAGES>() + 15) / 16) * 16 + (size_t)(1 + TOPK) * B * HS_STRIDE * 2;
+  return ((down_smem_fixed<FMT, STAGES, NG>() + 15) / 16) * 16 + (size_t)(1 + TOPK) * B * HS_STRIDE * 2;
 }
 
-template <int FMT, int STAGES>
-__global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p) {
+// CTA r owns output rows 16r..16r+15.  Slot u is consumed by warp group
+// u % NG (two warps: the two 256-column halves of K) and lands in stage
+// u % STAGES.  The parity wait on a stage's barrier is only sound if every use
+// of a stage is consumed by the same group, in order; hence STAGES % NG == 0.
+template <int FMT, int STAGES, int NG>
+__global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownParams p) {
+  static_assert(STAGES % NG == 0, "each stage must belong to one consumer group");
   using F = Fmt<FMT>;
   constexpr int TILE = F::DN_TILE;
+  constexpr int NCW = DnCfg<NG>::COMPUTE_WARPS;
+  constexpr int NT = DnCfg<NG>::THREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)STAGES * TILE);  // [8][128], 16-byte aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 8 * 128);
+  float* red = reinterpret_cast<float*>(smem + (size_t)STAGES * TILE);  // [NCW][128], 16-byte aligned
+  float* ts_s = red + NCW * 128;                                         // [NE][2]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ts_s + TSCALE_WORDS);
   uint64_t* empty = full + STAGES;
   int* hexp = reinterpret_cast<int*>(empty + STAGES);    // [8]
-  int* misc = hexp + 8;                                  // [0] abort, [1] n_pairs
+  int* misc = hexp + 8;                                  // [1] n_pairs
   uint8_t* pidx = reinterpret_cast<uint8_t*>(misc + 8);  // [MAX_SLOTS][8]
   uint8_t* psrc_tok = pidx + MAX_SLOTS * BMAX;           // [<= 56] token of pair
   uint8_t* psrc_slot = psrc_tok + 64;                    // [<= 56] slot of pair
   Routing& R = *reinterpret_cast<Routing*>(psrc_slot + 64);
-  uint16_t* hs = reinterpret_cast<uint16_t*>(smem + ((down_smem_fixed<FMT, STAGES>() + 15) / 16) * 16);
+  uint16_t* hs = reinterpret_cast<uint16_t*>(smem + ((down_smem_fixed<FMT, STAGES, NG>() + 15) / 16) * 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x;
   const int B = p.B;
+  if (FMT == 0)
+    for (int q = tid; q < NE * 2; q += NT) ts_s[q] = __ldg(p.tscale + q);  // constants
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 2);
     }
-    misc[0] = 0;
     fence_mbar_init();
   }
   pdl_trigger();  // the next sublayer's router only prefetches constants before its wait
@@ -570,7 +702,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
   const int n_slots = R.n_slots;
   const uint64_t pol = l2_evict_first();
   int issued = 0;
-  if (tid == 256) {
+  if (tid == NCW * 32) {
     for (; issued < STAGES && issued < n_slots; ++issued) {
       const int e = R.slot_expert[issued];
       mbar_arrive_expect_tx(&full[issued], TILE);
@@ -607,42 +739,53 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
     }
     if (lane == 0) misc[1] = base;
   }
+  __syncthreads();
+  const int n_pairs = misc[1];
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
 
+  // One round trip: every h row chunk is requested at once, together with the
+  // per-token maxima that set the f16 exponents.
+  for (int idx = tid; idx < n_pairs * 64; idx += NT) {
+    const int pr = idx >> 6, ch = idx & 63;
+    const int tk = psrc_tok[pr], u = psrc_slot[pr];
+    cp_async16(hs + (size_t)pr * HS_STRIDE + ch * 8, p.h + ((size_t)u * BMAX + tk) * I + ch * 8);
+  }
   if (FMT == 0 && warp < B) {
+    float v[MAX_HPARTS / 32];
+#pragma unroll
+    for (int j = 0; j < MAX_HPARTS / 32; ++j) {
+      const int q = lane + 32 * j;
+      v[j] = q < p.n_hparts ? __ldcg(p.hmax_part + (size_t)q * BMAX + warp) : 0.f;
+    }
     float m = 0.f;
-    for (int j = lane; j < p.n_hparts; j += 32) m = fmaxf(m, __ldcg(p.hmax_part + (size_t)j * BMAX + warp));
+#pragma unroll
+    for (int j = 0; j < MAX_HPARTS / 32; ++j) m = fmaxf(m, v[j]);
     const unsigned mb = redux_max(__float_as_uint(m));
     if (lane == 0) hexp[warp] = f16_range_exp(__uint_as_float(mb));
   }
+  cp_async_wait_all();
   __syncthreads();
-  {
-    const int n_pairs = misc[1];
-    for (int idx = tid; idx < n_pairs * 64; idx += DN_THREADS) {
+  if (FMT == 0) {
+    // bf16 h -> f16 h * 2^hexp[token], in place (each thread its own chunks).
+    for (int idx = tid; idx < n_pairs * 64; idx += NT) {
       const int pr = idx >> 6, ch = idx & 63;
-      const int tk = psrc_tok[pr], u = psrc_slot[pr];
-      const uint4 raw =
-          __ldcg(reinterpret_cast<const uint4*>(p.h + ((size_t)u * BMAX + tk) * I) + ch);
-      uint4 outv = raw;
-      if (FMT == 0) {
-        float f[8];
-        bf16x8_to_f32(raw, f);
-        const float sc = exp2i(hexp[tk]);
-        uint32_t pk[4];
+      uint4* ptr = reinterpret_cast<uint4*>(hs + (size_t)pr * HS_STRIDE + ch * 8);
+      float f[8];
+      bf16x8_to_f32(*ptr, f);
+      const float sc = exp2i(hexp[psrc_tok[pr]]);
+      uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 hv = __floats2half2_rn(__fmul_rn(f[2 * i], sc), __fmul_rn(f[2 * i + 1], sc));
-          pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
-        outv = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int i = 0; i < 4; ++i) {
+        const __half2 hv = __floats2half2_rn(__fmul_rn(f[2 * i], sc), __fmul_rn(f[2 * i + 1], sc));
+        pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      *reinterpret_cast<uint4*>(hs + (size_t)pr * HS_STRIDE + ch * 8) = outv;
+      *ptr = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
+    __syncthreads();
   }
-  __syncthreads();
 
-  if (warp == 8) {
+  if (warp == NCW) {
     if (lane == 0) {
       for (int n = issued; n < n_slots; ++n) {
         const int s = n % STAGES;
@@ -667,11 +810,10 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
   const int g = lane >> 2, t = lane & 3;
   const int kh = warp & 1, grp = warp >> 1;
   float tot[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int u = grp; u < n_slots; u += 4) {
+  for (int u = grp; u < n_slots; u += NG) {
     const int s = u % STAGES;
     if (!mbar_wait(&full[s], (u / STAGES) & 1)) {
       atomicOr(p.err, ERR_WAIT_FULL);
-      misc[0] = 1;
       break;
     }
     uint32_t bfr[16][2];
@@ -693,7 +835,7 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     const int e = R.slot_expert[u];
-    const float ts = FMT == 0 ? __ldg(p.tscale + 2 * e + 1) : 1.0f;
+    const float ts = FMT == 0 ? ts_s[2 * e + 1] : 1.0f;
     const float w0 = __fmul_rn(R.slot_w[u][2 * t], ts);
     const float w1 = __fmul_rn(R.slot_w[u][2 * t + 1], ts);
     tot[0] = fmaf(w0, acc[0], tot[0]);
@@ -701,53 +843,35 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
     tot[2] = fmaf(w0, acc[2], tot[2]);
     tot[3] = fmaf(w1, acc[3], tot[3]);
   }
-  *reinterpret_cast<float4*>(red + warp * 128 + lane * 4) = make_float4(tot[0], tot[1], tot[2], tot[3]);
-  named_bar_sync(1, 256);
-  if (warp == 0) {
-    float c[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) c[j] = red[lane * 4 + j];
+  for (int j = 0; j < 4; ++j) red[warp * 128 + j * 32 + lane] = tot[j];
+  named_bar_sync(1, NCW * 32);
+  if (tid < 128) {
+    // thread = (token tk, row): sum the warps' partials in a fixed order
+    const int row = tid & 15, tk = tid >> 4;
+    const int o = red_off(row, tk);
+    float c = 0.f;
 #pragma unroll
-    for (int w = 1; w < 8; ++w) {
-      const float4 v = *reinterpret_cast<const float4*>(red + w * 128 + lane * 4);
-      c[0] += v.x;
-      c[1] += v.y;
-      c[2] += v.z;
-      c[3] += v.w;
-    }
-    CSum sq[2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int tk = 2 * t + q;
-      if (tk < B) {
-        const float sc = FMT == 0 ? exp2i(-hexp[tk]) : 1.0f;
-        const __nv_bfloat16 y0 = __float2bfloat16_rn(__fmul_rn(c[q], sc));
-        const __nv_bfloat16 y1 = __float2bfloat16_rn(__fmul_rn(c[2 + q], sc));
-        const size_t o0 = (size_t)tk * H + rt * 16 + g;
-        p.y[o0] = y0;
-        p.y[o0 + 8] = y1;
-        if (p.y_copy) {
-          p.y_copy[o0] = y0;
-          p.y_copy[o0 + 8] = y1;
-        }
-        const float f0 = __bfloat162float(y0), f1 = __bfloat162float(y1);
-        cs_add(sq[q], __fmul_rn(f0, f0));
-        cs_add(sq[q], __fmul_rn(f1, f1));
-      }
+    for (int w = 0; w < NCW; ++w) c += red[w * 128 + o];
+    CSum sq = {0.f, 0.f};
+    if (tk < B) {
+      const float sc = FMT == 0 ? exp2i(-hexp[tk]) : 1.0f;
+      const __nv_bfloat16 yv = __float2bfloat16_rn(__fmul_rn(c, sc));
+      const size_t oy = (size_t)tk * H + rt * 16 + row;
+      p.y[oy] = yv;
+      if (p.y_copy) p.y_copy[oy] = yv;
+      const float f = __bfloat162float(yv);
+      sq.s = __fmul_rn(f, f);
     }
     if (p.ss_out) {
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        CSum a = sq[q];
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          CSum b;
-          b.s = __shfl_xor_sync(0xffffffffu, a.s, off);
-          b.c = __shfl_xor_sync(0xffffffffu, a.c, off);
-          cs_merge(a, b);
-        }
-        if (g == 0) p.ss_out[(size_t)rt * BMAX + 2 * t + q] = a;
+      for (int off = 1; off < 16; off <<= 1) {
+        CSum b;
+        b.s = __shfl_xor_sync(0xffffffffu, sq.s, off);
+        b.c = __shfl_xor_sync(0xffffffffu, sq.c, off);
+        cs_merge(sq, b);
       }
+      if (row == 0) p.ss_out[(size_t)rt * BMAX + tk] = sq;
     }
   }
 }
@@ -755,10 +879,14 @@ __global__ void __launch_bounds__(DN_THREADS, 1) down_kernel(const DownParams p)
 // ------------------------------------------------------------------ host side
 
 constexpr int F4_GU_STAGES = 5;
-constexpr int F4_DN_STAGES = 8;
 constexpr int B16_GU_STAGES = 3;
-constexpr int B16_DN_STAGES = 6;
-constexpr int ROUTER_EPC = 2;
+// Down kernel: 4 slot groups, small enough to be resident beside a gate/up
+// CTA so that its down tiles stream in while gate/up still runs.  With 8
+// tokens the staged h rows take 58 KB, so the tile ring shrinks to 8 stages.
+constexpr int DN_GROUPS = 4;
+constexpr int F4_DN_STAGES_S = 12, F4_DN_STAGES_L = 8;  // B <= 4 / B > 4
+constexpr int B16_DN_STAGES = 4;
+constexpr int DN_SMALL_MAX_B = 4;
 
 static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -766,7 +894,8 @@ size_t decode_ws_bytes(int gu_grid) {
   size_t b = 0;
   b += align256((size_t)BMAX * E * 2);                  // logits
   b += align256((size_t)BMAX * H * 2);                  // xh_bf16
-  b += align256((size_t)BMAX * H * 2);                  // xh_f16
+  b += align256((size_t)XFRAG_WORDS * 4);               // xfrag_f16
+  b += align256((size_t)XFRAG_WORDS * 4);               // xfrag_bf16
   b += align256(BMAX * 4);                              // xh_exp
   b += align256((size_t)MAX_SLOTS * BMAX * I * 2);      // h
   b += align256((size_t)gu_grid * BMAX * 4);            // hmax_part
@@ -782,8 +911,10 @@ DecodeWs carve_decode_ws(void* ws, int gu_grid) {
   p += align256((size_t)BMAX * E * 2);
   w.xh_bf16 = p;
   p += align256((size_t)BMAX * H * 2);
-  w.xh_f16 = p;
-  p += align256((size_t)BMAX * H * 2);
+  w.xfrag_f16 = p;
+  p += align256((size_t)XFRAG_WORDS * 4);
+  w.xfrag_bf16 = p;
+  p += align256((size_t)XFRAG_WORDS * 4);
   w.xh_exp = reinterpret_cast<int*>(p);
   p += align256(BMAX * 4);
   w.h = p;
@@ -812,9 +943,24 @@ static cudaError_t launch(void (*k)(KArgs...), int grid, int block, size_t smem,
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
+// One expert per CTA (256 CTAs) while the per-thread state is small; two
+// experts per CTA (128 CTAs, one wave beside the waiting gate/up CTAs) when
+// the batch makes every CTA register-heavy.
+template <int NB>
+struct RouterEpc {
+  static constexpr int value = NB <= 2 ? 1 : 2;
+};
+
 template <int NB>
 static cudaError_t launch_router_nb(const RouterParams& rp, cudaStream_t st, bool pdl) {
-  return launch(router_kernel<ROUTER_EPC, NB>, E / ROUTER_EPC, 256, 0, st, pdl, rp);
+  constexpr int EPC = RouterEpc<NB>::value;
+  return launch(router_kernel<NB, EPC>, E / EPC, 256, 0, st, pdl, rp);
+}
+
+template <int NB>
+static cudaError_t router_carveout() {
+  return cudaFuncSetAttribute(router_kernel<NB, RouterEpc<NB>::value>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 static cudaError_t launch_router(int B, const RouterParams& rp, cudaStream_t st, bool pdl) {
@@ -831,20 +977,35 @@ static cudaError_t launch_router(int B, const RouterParams& rp, cudaStream_t st,
   }
 }
 
+// Every kernel asks for the maximal shared-memory carveout: an SM can only
+// host CTAs of kernels with the same L1/shared split, and the chained kernels
+// of a sublayer are meant to be resident together (a dependent kernel's
+// prologue prefetches while its predecessor runs).
+template <typename K>
+static cudaError_t set_smem(K k, size_t bytes) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
 cudaError_t decode_kernels_init(int /*device*/) {
   cudaError_t e;
-  e = cudaFuncSetAttribute(gateup_kernel<0, F4_GU_STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)gateup_smem_bytes<0, F4_GU_STAGES>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gateup_kernel<1, B16_GU_STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)gateup_smem_bytes<1, B16_GU_STAGES>());
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(down_kernel<0, F4_DN_STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)down_smem_bytes<0, F4_DN_STAGES>(BMAX));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(down_kernel<1, B16_DN_STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)down_smem_bytes<1, B16_DN_STAGES>(BMAX));
-  return e;
+  if ((e = set_smem(gateup_kernel<0, F4_GU_STAGES>, gateup_smem_bytes<0, F4_GU_STAGES>())) != cudaSuccess) return e;
+  if ((e = set_smem(gateup_kernel<1, B16_GU_STAGES>, gateup_smem_bytes<1, B16_GU_STAGES>())) != cudaSuccess) return e;
+  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>,
+                    down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(DN_SMALL_MAX_B))) != cudaSuccess)
+    return e;
+  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(BMAX))) !=
+      cudaSuccess)
+    return e;
+  if ((e = set_smem(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(BMAX))) !=
+      cudaSuccess)
+    return e;
+  cudaError_t r[8] = {router_carveout<1>(), router_carveout<2>(), router_carveout<3>(), router_carveout<4>(),
+                      router_carveout<5>(), router_carveout<6>(), router_carveout<7>(), router_carveout<8>()};
+  for (cudaError_t x : r)
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, const void* ss_in, int B, float eps,
@@ -859,7 +1020,8 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   rp.want_f16 = fmt == 0;
   rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
   rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
-  rp.xh_f16 = static_cast<__half*>(ws.xh_f16);
+  rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);
+  rp.xfrag_bf16 = static_cast<uint32_t*>(ws.xfrag_bf16);
   rp.xh_exp = ws.xh_exp;
   cudaError_t e = launch_router(B, rp, st, pdl_first);
   if (e != cudaSuccess) return e;
@@ -868,7 +1030,7 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   gp.experts = L.experts;
   gp.tscale = L.tscale;
   gp.logits = rp.logits;
-  gp.xh = fmt == 0 ? static_cast<const void*>(ws.xh_f16) : static_cast<const void*>(ws.xh_bf16);
+  gp.xfrag = fmt == 0 ? rp.xfrag_f16 : rp.xfrag_bf16;
   gp.xh_exp = ws.xh_exp;
   gp.B = B;
   gp.h = static_cast<__nv_bfloat16*>(ws.h);
@@ -896,12 +1058,18 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   dp.y_copy = static_cast<__nv_bfloat16*>(ys_copy);
   dp.ss_out = static_cast<CSum*>(ss_out);
   dp.err = err;
-  if (fmt == 0)
-    e = launch(down_kernel<0, F4_DN_STAGES>, DN_TILES, DN_THREADS, down_smem_bytes<0, F4_DN_STAGES>(B), st, true,
-               dp);
-  else
-    e = launch(down_kernel<1, B16_DN_STAGES>, DN_TILES, DN_THREADS, down_smem_bytes<1, B16_DN_STAGES>(B), st,
-               true, dp);
+  constexpr int NT = DnCfg<DN_GROUPS>::THREADS;
+  if (fmt == 0) {
+    if (B <= DN_SMALL_MAX_B)
+      e = launch(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>, DN_TILES, NT,
+                 down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(B), st, true, dp);
+    else
+      e = launch(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, DN_TILES, NT,
+                 down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(B), st, true, dp);
+  } else {
+    e = launch(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, DN_TILES, NT, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(B),
+               st, true, dp);
+  }
   return e;
 }
 

@@ -148,7 +148,7 @@ __device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s) {
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -156,7 +156,7 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 }
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -172,6 +172,39 @@ __device__ __forceinline__ unsigned redux_min(unsigned v) {
   unsigned r;
   asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
   return r;
+}
+
+// Asynchronous 16-byte global -> shared copies (L2 only), completed per thread.
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n cp.async.wait_all;" ::: "memory");
+}
+
+// Packed fp32 pairs (sm_100+): two IEEE round-to-nearest operations per instruction.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // ------------------------------------------------------- compensated summation
@@ -205,6 +238,22 @@ __device__ __forceinline__ CSum cs_warp_reduce(CSum x) {
 }
 __device__ __forceinline__ float cs_value(const CSum& x) { return __fadd_rn(x.s, x.c); }
 
+// Two independent compensated sums in packed fp32 pairs (same TwoSum steps).
+struct CSum2 {
+  uint64_t s, c;
+};
+__device__ __forceinline__ void cs2_add(CSum2& x, uint64_t p) {
+  const uint64_t s = f2add(x.s, p);
+  const uint64_t z = f2sub(s, x.s);
+  const uint64_t e = f2add(f2sub(x.s, f2sub(s, z)), f2sub(p, z));
+  x.s = s;
+  x.c = f2add(x.c, e);
+}
+__device__ __forceinline__ void cs2_split(const CSum2& x, CSum& lo, CSum& hi) {
+  f2unpack(x.s, lo.s, hi.s);
+  f2unpack(x.c, lo.c, hi.c);
+}
+
 // ---------------------------------------------------------------- routing
 // Result of sigmoid top-6 for a batch, laid out for the expert kernels.
 // Slot 0 is the shared expert; slots 1..n_slots-1 are the distinct routed
@@ -220,107 +269,167 @@ struct Routing {
   int ubase[8];                   // exclusive prefix of popc(umask)
 };
 
-// Computes the routing of B tokens from bf16 logits [B][256] (global memory,
-// written by the router kernel of the same sublayer).  Must be called by all
-// threads of a block of at least 8 warps; ends with __syncthreads.
+// Sigmoid top-6 of one token by one warp.  Lane l holds experts 8l..8l+7 of
+// the bf16 logits row (global memory, written by the router kernel):
 //   s = 1 / (1 + exp(-logit)) in fp32; top-6 by s, ties to the lower index;
-//   w_j = s_j / sum of the 6 selected s.
-__device__ __forceinline__ void compute_routing(const __nv_bfloat16* __restrict__ logits, int B, Routing& r) {
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < MAX_SLOTS * (BMAX + 2); i += blockDim.x) {
-    const int s = i / (BMAX + 2), k = i % (BMAX + 2);
-    if (k < BMAX) r.slot_w[s][k] = 0.f;
-    else if (k == BMAX) r.slot_mask[s] = 0u;
-    else r.slot_expert[s] = -1;
+//   w_j = s_j / sum of the 6 selected s (fp32, summed in selection order).
+// Fast path: for bf16 logits v with 2^-12 <= |v|, -80 < v < 8, the correctly
+// rounded fp32 sigmoid of v exceeds that of the next smaller bf16 value by at
+// least 4 fp32 ulps (checked exhaustively over all bf16 values); outside that
+// band fp32 scores of distinct logits can coincide (s rounds to 0.5 near 0,
+// to 1 above ~17, underflows below ~-87).  So if all 7 best candidates by
+// (logit desc, index asc) lie in the band, that order equals the order by
+// (s desc, index asc) exactly, and a 32-bit key (order-preserving logit bits,
+// then 255 - index) selects with one warp max per pick.  Otherwise the
+// selection is redone on the fp32 scores.  Lanes 0..5 store ids and weights.
+__device__ __forceinline__ uint4 load_logits(const __nv_bfloat16* __restrict__ row, int lane) {
+  return __ldcg(reinterpret_cast<const uint4*>(row) + lane);
+}
+__device__ __forceinline__ float sigmoid_f32(float lg) { return __frcp_rn(__fadd_rn(1.0f, expf(-lg))); }
+
+__device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_out, float* w_out,
+                                          uint32_t* umask) {
+  const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+  uint32_t hb[8], key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    hb[i] = (wv[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
+    const uint32_t ord = (hb[i] & 0x8000u) ? (~hb[i] & 0xFFFFu) : (hb[i] | 0x8000u);
+    key[i] = (ord << 16) | (255u - (uint32_t)(lane * 8 + i));
   }
-  if (tid < 8) r.umask[tid] = 0u;
-  __syncthreads();
-  if (warp < B) {
-    const uint4 raw = __ldcg(reinterpret_cast<const uint4*>(logits + (size_t)warp * E) + lane);
-    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+  // Fast path: top-7 by key (the 7th only to bound the candidates).
+  uint32_t taken = 0u, sel_key[TOPK + 1];
+#pragma unroll
+  for (int k = 0; k < TOPK + 1; ++k) {
+    uint32_t best = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (!((taken >> i) & 1u) && key[i] > best) best = key[i];
+    const uint32_t m = redux_max(best);
+    const uint32_t idx = 255u - (m & 0xFFu);
+    if ((idx >> 3) == (uint32_t)lane) taken |= 1u << (idx & 7u);
+    sel_key[k] = m;
+  }
+  bool exact_by_logit = true;
+#pragma unroll
+  for (int k = 0; k < TOPK + 1; ++k) {
+    const uint32_t ord = sel_key[k] >> 16;
+    const uint32_t bits = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
+    const uint32_t mag = bits & 0x7FFFu;  // 0x3980 = 2^-12, 0x4100 = 8, 0x42A0 = 80
+    const bool in_band = mag >= 0x3980u && ((bits & 0x8000u) ? mag < 0x42A0u : mag < 0x4100u);
+    exact_by_logit = exact_by_logit && in_band;
+  }
+  float sel_s[TOPK];
+  int sel_i[TOPK];
+  if (exact_by_logit) {
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k) {
+      const uint32_t ord = sel_key[k] >> 16;
+      const uint32_t bits = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
+      sel_i[k] = 255 - (int)(sel_key[k] & 0xFFu);
+      sel_s[k] = sigmoid_f32(__uint_as_float(bits << 16));
+    }
+  } else {
     uint32_t bits[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t hb = (wv[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu;
-      const float lg = __uint_as_float(hb << 16);
-      const float s = __frcp_rn(__fadd_rn(1.0f, expf(-lg)));
-      bits[i] = __float_as_uint(s);
-    }
-    uint32_t taken = 0u;
-    float sel_s[TOPK];
-    int sel_i[TOPK];
+    for (int i = 0; i < 8; ++i) bits[i] = __float_as_uint(sigmoid_f32(__uint_as_float(hb[i] << 16)));
+    uint32_t tk2 = 0u;
 #pragma unroll
     for (int k = 0; k < TOPK; ++k) {
       uint32_t best = 0u, bidx = 0xFFFFFFFFu;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (!((taken >> i) & 1u) && (bidx == 0xFFFFFFFFu || bits[i] > best)) {
+        if (!((tk2 >> i) & 1u) && (bidx == 0xFFFFFFFFu || bits[i] > best)) {
           best = bits[i];
           bidx = lane * 8 + i;
         }
       }
       const uint32_t m = redux_max(best);
       const uint32_t win = redux_min(best == m ? bidx : 0xFFFFFFFFu);
-      if ((win >> 3) == (uint32_t)lane) taken |= 1u << (win & 7u);
+      if ((win >> 3) == (uint32_t)lane) tk2 |= 1u << (win & 7u);
       sel_s[k] = __uint_as_float(m);
       sel_i[k] = (int)win;
     }
-    float sum = 0.f;
-#pragma unroll
-    for (int k = 0; k < TOPK; ++k) sum = __fadd_rn(sum, sel_s[k]);
-    if (lane < TOPK) {
-      float ws = 0.f;
-      int wi = 0;
-#pragma unroll
-      for (int k = 0; k < TOPK; ++k)
-        if (k == lane) {
-          ws = sel_s[k];
-          wi = sel_i[k];
-        }
-      r.ids[warp][lane] = wi;
-      r.w[warp][lane] = __fdiv_rn(ws, sum);
-      atomicOr(&r.umask[wi >> 5], 1u << (wi & 31));
-    }
   }
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t m = lane < 8 ? r.umask[lane] : 0u;
-    const int cnt = __popc(m);
-    int incl = cnt;
+  float sum = 0.f;
 #pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += v;
-    }
-    const int base = incl - cnt;
-    if (lane < 8) {
-      r.ubase[lane] = base;
-      uint32_t mm = m;
-      int j = 0;
-      while (mm) {
-        const int b = __ffs(mm) - 1;
-        mm &= mm - 1;
-        r.slot_expert[1 + base + j] = lane * 32 + b;
-        ++j;
+  for (int k = 0; k < TOPK; ++k) sum = __fadd_rn(sum, sel_s[k]);
+  if (lane < TOPK) {
+    float ws = 0.f;
+    int wi = 0;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k)
+      if (k == lane) {
+        ws = sel_s[k];
+        wi = sel_i[k];
       }
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 7);
-    if (lane == 0) {
-      r.n_slots = 1 + total;
-      r.slot_expert[0] = E;
-      r.slot_mask[0] = (B >= 32) ? 0xFFFFFFFFu : ((1u << B) - 1u);
-    }
-    if (lane < B) r.slot_w[0][lane] = 1.0f;
+    ids_out[lane] = wi;
+    w_out[lane] = __fdiv_rn(ws, sum);
+    atomicOr(&umask[wi >> 5], 1u << (wi & 31));
   }
-  __syncthreads();
-  if (warp < B && lane < TOPK) {
-    const int e = r.ids[warp][lane];
+}
+
+// Builds the slot table from the per-token selections (one warp).  Slot 0 is
+// the shared expert; slots 1.. are the distinct routed experts in ascending
+// order.  Requires r.umask/ids/w complete and slot_w/slot_mask zeroed.
+__device__ __forceinline__ void warp_slot_table(Routing& r, int B, int lane) {
+  const uint32_t m = lane < 8 ? r.umask[lane] : 0u;
+  const int cnt = __popc(m);
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  const int base = incl - cnt;
+  if (lane < 8) {
+    r.ubase[lane] = base;
+    uint32_t mm = m;
+    int j = 0;
+    while (mm) {
+      const int b = __ffs(mm) - 1;
+      mm &= mm - 1;
+      r.slot_expert[1 + base + j] = lane * 32 + b;
+      ++j;
+    }
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 7);
+  if (lane == 0) {
+    r.n_slots = 1 + total;
+    r.slot_expert[0] = E;
+    r.slot_mask[0] = (1u << B) - 1u;
+  }
+  if (lane < B) r.slot_w[0][lane] = 1.0f;
+  __syncwarp();
+  for (int q = lane; q < B * TOPK; q += 32) {
+    const int t = q / TOPK, j = q % TOPK;
+    const int e = r.ids[t][j];
     const int wd = e >> 5;
     const int slot = 1 + r.ubase[wd] + __popc(r.umask[wd] & ((1u << (e & 31)) - 1u));
-    r.slot_w[slot][warp] = r.w[warp][lane];
-    atomicOr(&r.slot_mask[slot], 1u << warp);
+    r.slot_w[slot][t] = r.w[t][j];
+    atomicOr(&r.slot_mask[slot], 1u << t);
   }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void zero_routing(Routing& r, int tid, int nthreads) {
+  for (int i = tid; i < MAX_SLOTS * (BMAX + 2); i += nthreads) {
+    const int s = i / (BMAX + 2), k = i % (BMAX + 2);
+    if (k < BMAX) r.slot_w[s][k] = 0.f;
+    else if (k == BMAX) r.slot_mask[s] = 0u;
+    else r.slot_expert[s] = -1;
+  }
+  if (tid < 8) r.umask[tid] = 0u;
+}
+
+// Full routing of B tokens by a block of >= 8 warps; ends with __syncthreads.
+__device__ __forceinline__ void compute_routing(const __nv_bfloat16* __restrict__ logits, int B, Routing& r) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  zero_routing(r, tid, blockDim.x);
+  __syncthreads();
+  if (warp < B) warp_topk(load_logits(logits + (size_t)warp * E, lane), lane, r.ids[warp], r.w[warp], r.umask);
+  __syncthreads();
+  if (warp == 0) warp_slot_table(r, B, lane);
   __syncthreads();
 }
 

@@ -13,7 +13,8 @@ namespace flint {
 struct DecodeWs {
   void* logits;      // bf16 [8][256]
   void* xh_bf16;     // bf16 [8][2048]
-  void* xh_f16;      // f16  [8][2048] (x_hat * 2^xh_exp[token])
+  void* xfrag_f16;   // f16 x_hat * 2^xh_exp[token], mma B-fragment order
+  void* xfrag_bf16;  // bf16 x_hat, mma B-fragment order
   int* xh_exp;       // [8]
   void* h;           // bf16 [49 slots][8 tokens][512]
   float* hmax_part;  // [gate/up grid][8]

@@ -30,16 +30,38 @@ def f64_to_bf16_tensor(a: np.ndarray, device="cpu") -> torch.Tensor:
     return torch.from_numpy(bits.copy()).view(torch.bfloat16).to(device)
 
 
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 7)
+
+
+SLACK_FRACTION = 0.01
+
+
 def check_output(got: np.ndarray, ref: np.ndarray, what: str = "y"):
+    """max|err| <= 2e-2 * rms and mean|err| <= 2e-3 * rms (rms of the oracle output).
+
+    Both sides round to bf16, and two correct results can differ by one bf16 ulp
+    where the exact value sits near a rounding midpoint: for |ref| > 2.56 * rms that
+    ulp alone exceeds 2e-2 * rms.  So an element may exceed the max bound by being
+    at most one ulp of the reference away, and at most 1% of the elements may use
+    that slack.
+    """
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     rms = float(np.sqrt(np.mean(ref * ref)))
     err = np.abs(got - ref)
-    assert err.max() <= MAX_REL * rms, f"{what}: max|err| {err.max():.4g} > {MAX_REL} * rms {rms:.4g}"
+    bound = np.maximum(MAX_REL * rms, bf16_ulp(ref))
+    over = err > MAX_REL * rms
+    worst = float(np.max(err / bound))
+    assert worst <= 1.0, f"{what}: max|err| {err.max():.4g} beyond max(2e-2*rms={MAX_REL * rms:.4g}, 1 ulp)"
+    assert over.mean() <= SLACK_FRACTION, f"{what}: {over.mean():.3%} of elements beyond 2e-2*rms"
     assert err.mean() <= MEAN_REL * rms, f"{what}: mean|err| {err.mean():.4g} > {MEAN_REL} * rms {rms:.4g}"
-    return dict(max_rel=float(err.max() / rms), mean_rel=float(err.mean() / rms), rms=rms)
+    return dict(max_rel=float(err.max() / rms), mean_rel=float(err.mean() / rms), rms=rms,
+                n_over_strict=int(over.sum()), frac_differ=float(np.mean(err > 0)))
 
 
 def valid_near_tie_selection(scores: np.ndarray, ids, tol: float = GAP_TOL) -> bool:
