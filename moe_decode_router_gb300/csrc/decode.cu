@@ -489,6 +489,9 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   }
 
   pdl_wait();
+  // The down kernel may start now: before its own dependency wait it reads
+  // only the router's logits, which are final once this wait has returned.
+  pdl_trigger();
   const int g = lane >> 2;
   // The routing input first: the top-k waits on it, the B fragments are needed later.
   uint4 lraw = make_uint4(0u, 0u, 0u, 0u);
@@ -512,7 +515,6 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   }
   if (warp < B) warp_topk(lraw, lane, R.ids[warp], R.w[warp], R.umask);
   __syncthreads();
-  pdl_trigger();  // the down kernel may start: the routing inputs are final
   int n_slots = 1;
 #pragma unroll
   for (int i = 0; i < 8; ++i) n_slots += __popc(R.umask[i]);
@@ -684,8 +686,19 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rt = blockIdx.x;
   const int B = p.B;
-  if (FMT == 0)
-    for (int q = tid; q < NE * 2; q += NT) ts_s[q] = __ldg(p.tscale + q);  // constants
+  pdl_trigger();  // the next sublayer's router only prefetches constants before its wait
+  // The routing of this sublayer is final: this kernel is launched only after
+  // every gate/up CTA passed its dependency wait on the router.  Issue every
+  // independent load first (tensor scales, logits), then consume them.
+  constexpr int TS_PER_T = (NE * 2 + NT - 1) / NT;
+  float tsv[TS_PER_T];
+#pragma unroll
+  for (int j = 0; j < TS_PER_T; ++j) {
+    const int q = tid + j * NT;
+    tsv[j] = (FMT == 0 && q < NE * 2) ? __ldg(p.tscale + q) : 0.f;
+  }
+  uint4 lraw = make_uint4(0u, 0u, 0u, 0u);
+  if (warp < B) lraw = load_logits(p.logits + (size_t)warp * E, lane);
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
@@ -694,28 +707,23 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
     }
     fence_mbar_init();
   }
-  pdl_trigger();  // the next sublayer's router only prefetches constants before its wait
-  __syncthreads();
-  // The routing of this sublayer is final: this kernel is launched only after
-  // every gate/up CTA passed its dependency wait on the router.
-  compute_routing(p.logits, B, R);
-  const int n_slots = R.n_slots;
-  const uint64_t pol = l2_evict_first();
-  int issued = 0;
-  if (tid == NCW * 32) {
-    for (; issued < STAGES && issued < n_slots; ++issued) {
-      const int e = R.slot_expert[issued];
-      mbar_arrive_expect_tx(&full[issued], TILE);
-      bulk_g2s(stages + (size_t)issued * TILE, p.experts + (size_t)e * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE,
-               TILE, &full[issued], pol);
-    }
+  zero_routing(R, tid, NT);
+#pragma unroll
+  for (int j = 0; j < TS_PER_T; ++j) {
+    const int q = tid + j * NT;
+    if (q < NE * 2) ts_s[q] = tsv[j];
   }
+  __syncthreads();
+  if (warp < B) warp_topk(lraw, lane, R.ids[warp], R.w[warp], R.umask);
+  __syncthreads();
   if (warp == 0) {
+    warp_slot_table(R, B, lane);
     // compact (slot, token) pairs: pair index = prefix over slots of popc(mask)
+    const int n_slots_w = R.n_slots;
     int base = 0;
-    for (int c0 = 0; c0 < n_slots; c0 += 32) {
+    for (int c0 = 0; c0 < n_slots_w; c0 += 32) {
       const int u = c0 + lane;
-      const uint32_t m = u < n_slots ? R.slot_mask[u] : 0u;
+      const uint32_t m = u < n_slots_w ? R.slot_mask[u] : 0u;
       const int cnt = __popc(m);
       int incl = cnt;
 #pragma unroll
@@ -724,7 +732,7 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
         if (lane >= off) incl += v;
       }
       int pi = base + incl - cnt;
-      if (u < n_slots) {
+      if (u < n_slots_w) {
 #pragma unroll
         for (int tk = 0; tk < BMAX; ++tk) {
           if ((m >> tk) & 1u) {
@@ -741,6 +749,17 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   }
   __syncthreads();
   const int n_pairs = misc[1];
+  const int n_slots = R.n_slots;
+  const uint64_t pol = l2_evict_first();
+  int issued = 0;
+  if (tid == NCW * 32) {
+    for (; issued < STAGES && issued < n_slots; ++issued) {
+      const int e = R.slot_expert[issued];
+      mbar_arrive_expect_tx(&full[issued], TILE);
+      bulk_g2s(stages + (size_t)issued * TILE, p.experts + (size_t)e * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE,
+               TILE, &full[issued], pol);
+    }
+  }
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
 
