@@ -156,6 +156,36 @@ int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *l
                             float *topk_w, void *ws, size_t ws_bytes,
                             flint_moe_stream_t stream);
 
+/* Size of the scratch area built into the library for
+ * flint_moe_decode_layer_noalloc, and the largest batch it serves. */
+#define FLINT_MOE_NOALLOC_SCRATCH_BYTES 589824
+#define FLINT_MOE_NOALLOC_MAX_TOKENS 8
+
+/*
+ * flint_moe_decode_layer without a workspace argument, for callers that
+ * cannot allocate device memory: code that runs where cudaMalloc is not
+ * allowed or not wanted (inside a host callback or another library's
+ * allocator hook, under a strict memory budget, or from a runtime that owns
+ * every device allocation itself).  The paper has no counterpart; this is a
+ * convenience of this library.
+ *
+ * Scratch lives in one fixed array of FLINT_MOE_NOALLOC_SCRATCH_BYTES in the
+ * library's device image: every GPU that loads the library holds it until the
+ * process exits, and this call allocates nothing.  Inputs, outputs and
+ * weights are as for flint_moe_decode_layer (caller-owned device memory).
+ *   B > FLINT_MOE_NOALLOC_MAX_TOKENS returns FLINT_MOE_ERR_WORKSPACE (the
+ *   built-in scratch holds at most 8 tokens) and enqueues nothing.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array and it keeps the previous call's
+ * contents; the kernels read no scratch word they have not written in the
+ * same call, so nothing needs clearing.  Calls whose work overlaps on the GPU
+ * (different streams, or other threads) race on the array: order them.
+ */
+int flint_moe_decode_layer_noalloc(const flint_moe_dims *dims, const flint_moe_layer *layer,
+                                   const void *x, int B, void *y, int32_t *topk_ids,
+                                   float *topk_w, flint_moe_stream_t stream);
+
 /* Frees cached CUDA graphs of every device the calling thread used.  Call
  * before freeing buffers whose addresses a cached stack graph holds. */
 int flint_moe_release(void);

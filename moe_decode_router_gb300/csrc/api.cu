@@ -98,6 +98,46 @@ LayerArgs layer_args(const flint_moe_layer& L) {
 
 size_t decode_ws_needed() { return decode_ws_bytes(MAX_GU_GRID); }
 
+// Scratch of flint_moe_decode_layer_noalloc: one fixed array in the device
+// image (held by every GPU that loads the library, for the whole process).
+// In host code its name is only a stand-in; kernels get the device address
+// looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FLINT_MOE_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocState {
+  bool ready = false;
+  int gu_grid = 0;
+  unsigned* err = nullptr;
+  void* scratch = nullptr;
+};
+std::map<int, NoallocState> g_noalloc;
+
+// Once per device, with that device current; creates nothing and allocates
+// nothing.  Called with g_mu held.
+int noalloc_state(NoallocState** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  NoallocState& s = g_noalloc[dev];
+  if (!s.ready) {
+    int sms = 0, major = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (major != 10) return FLINT_MOE_ERR_UNSUPPORTED;
+    if (decode_ws_bytes(MAX_GU_GRID) > sizeof(g_noalloc_scratch)) return FLINT_MOE_ERR_WORKSPACE;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return FLINT_MOE_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_flint_error) != cudaSuccess)
+      return FLINT_MOE_ERR_CUDA;
+    if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    s.scratch = ptr;
+    s.gu_grid = sms < MAX_GU_GRID ? sms : MAX_GU_GRID;
+    s.ready = true;
+  }
+  *out = &s;
+  return FLINT_MOE_OK;
+}
+
 }  // namespace
 }  // namespace flint
 
@@ -237,6 +277,25 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
   }
   ds->graphs.push_back(GraphEntry{std::move(key), exec});
   return to_status(cudaGraphLaunch(exec, user));
+}
+
+int flint_moe_decode_layer_noalloc(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int B,
+                                   void* y, int32_t* topk_ids, float* topk_w, flint_moe_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != FLINT_MOE_OK) return st;
+  if ((st = check_layer(dims, layer)) != FLINT_MOE_OK) return st;
+  if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (B > FLINT_MOE_NOALLOC_MAX_TOKENS) return FLINT_MOE_ERR_WORKSPACE;  // beyond the built-in scratch
+  if (x == nullptr || y == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoallocState* ns = nullptr;
+  if ((st = noalloc_state(&ns)) != FLINT_MOE_OK) return st;
+  const DecodeWs w = carve_decode_ws(ns->scratch, MAX_GU_GRID);
+  return to_status(launch_decode_layer(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, layer_args(*layer), x,
+                                       nullptr, B, dims->rms_eps, y, nullptr, nullptr, topk_ids, topk_w, w,
+                                       ns->gu_grid, ns->err, reinterpret_cast<cudaStream_t>(stream), true));
 }
 
 int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int T, void* y,

@@ -71,6 +71,9 @@ _SIGS = {
     "flint_moe_prefill_layer": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(Layer), ctypes.c_void_p,
                                                ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "flint_moe_decode_layer_noalloc": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(Layer), ctypes.c_void_p,
+                                                      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                      ctypes.c_void_p]),
     "flint_moe_release": (ctypes.c_int, []),
     "flint_moe_device_error": (ctypes.c_int, [ctypes.c_int]),
     "flint_moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -190,6 +193,19 @@ def decode_layer(layer: FlintLayer, x, y, ws, topk_ids=None, topk_w=None, rms_ep
     rc = _lib().flint_moe_decode_layer(ctypes.byref(d), ctypes.byref(L), _ptr(x), B, _ptr(y), _ptr(topk_ids),
                                        _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "flint_moe_decode_layer")
+
+
+def decode_layer_noalloc(layer: FlintLayer, x, y, topk_ids=None, topk_w=None, rms_eps=1e-6, stream=None):
+    """decode_layer with the library's built-in scratch instead of a caller workspace.
+
+    For callers that cannot allocate device memory.  Calls on one device share
+    that scratch, so they must not overlap on the GPU.
+    """
+    d = dims(layer.weight_dtype, rms_eps)
+    L = layer.c_struct()
+    rc = _lib().flint_moe_decode_layer_noalloc(ctypes.byref(d), ctypes.byref(L), _ptr(x), x.shape[0], _ptr(y),
+                                               _ptr(topk_ids), _ptr(topk_w), _stream(stream))
+    _check(rc, "flint_moe_decode_layer_noalloc")
 
 
 def decode_stack(layers, x, y, ws, ids_per_layer=None, w_per_layer=None, ys_per_layer=None, rms_eps=1e-6,
