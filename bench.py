@@ -164,6 +164,32 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ----------------------------------------------------------------------------- ncu traffic
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("moe_decode_router_gb300/csrc/decode.cu", "moe_decode_router_gb300/csrc/flint_common.cuh"):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic_ratio(workload: str):
+    """DRAM traffic / algorithmic bytes of one sublayer from the committed ncu summary,
+    or None if there is none for this workload or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "decode_kernels_full_b1_b8.md")
+    if not os.path.exists(path):
+        return None, None
+    src = kernel_source_hash()
+    for line in open(path):
+        if line.startswith("flint-traffic "):
+            kv = dict(t.split("=", 1) for t in line.split()[1:])
+            if kv.get("workload") == workload and kv.get("source") == src:
+                return float(kv["ratio"]), os.path.relpath(path, ROOT)
+    return None, None
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def build_stack(F, synth, torch, wl, dev, n_layers):
@@ -283,6 +309,7 @@ def run_ours(args):
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     bytes_per_layer = total_bytes / args.steps / NL
+    traffic_ratio, traffic_src = profiled_traffic_ratio(args.workload)
     out = {
         "metric": METRIC,
         "value": round(us_per_layer, 3),
@@ -308,7 +335,9 @@ def run_ours(args):
             "kernel": "decode sublayer (router + gate/up + down, chained by programmatic dependent launch)",
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "peak_source": peak_src,
-            "bytes_per_layer": round(bytes_per_layer), "traffic": None,
+            "bytes_per_layer": round(bytes_per_layer),
+            "traffic": round(traffic_ratio * bytes_per_layer) if traffic_ratio else None,
+            "traffic_source": traffic_src,
         },
         "e2e": {"value": round(e2e_ms * 1000.0 / NL, 3), "unit": "us/layer",
                 "h2d_bytes_per_step": B * 2048 * 2, "d2h_bytes_per_step": B * 2048 * 2},
