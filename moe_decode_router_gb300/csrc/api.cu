@@ -57,6 +57,7 @@ int device_state(DeviceState** out) {
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_flint_error) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
     if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (prefill_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&s.capture_stream, cudaStreamNonBlocking) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
     s.ready = true;
@@ -97,6 +98,10 @@ LayerArgs layer_args(const flint_moe_layer& L) {
 }
 
 size_t decode_ws_needed() { return decode_ws_bytes(MAX_GU_GRID); }
+
+// Largest token count of one prefill call (keeps every pair index and
+// work-item count far inside int32).
+constexpr int PREFILL_MAX_TOKENS = 1 << 20;
 
 // Scratch of flint_moe_decode_layer_noalloc: one fixed array in the device
 // image (held by every GPU that loads the library, for the whole process).
@@ -152,8 +157,11 @@ size_t flint_moe_packed_bytes(const flint_moe_dims* dims) {
 
 size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int max_tokens) {
   if (check_dims(dims) != FLINT_MOE_OK || max_tokens < 1) return 0;
-  if (max_tokens <= BMAX) return decode_ws_needed();
-  return 0;  // prefill workspace: not available in this build
+  if (max_tokens > PREFILL_MAX_TOKENS) return 0;
+  const size_t dec = decode_ws_needed();
+  if (dims->weight_dtype != FLINT_MOE_W_NVFP4) return max_tokens <= BMAX ? dec : 0;  // prefill: NVFP4 only
+  const size_t pre = prefill_ws_bytes(max_tokens);
+  return pre > dec ? pre : dec;
 }
 
 int flint_moe_pack_weights(const flint_moe_dims* dims, const void* gate_up, const uint8_t* gate_up_scales,
@@ -300,18 +308,21 @@ int flint_moe_decode_layer_noalloc(const flint_moe_dims* dims, const flint_moe_l
 
 int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int T, void* y,
                             int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes, flint_moe_stream_t stream) {
-  (void)layer;
-  (void)x;
-  (void)T;
-  (void)y;
-  (void)topk_ids;
-  (void)topk_w;
-  (void)ws;
-  (void)ws_bytes;
-  (void)stream;
   int st = check_dims(dims);
   if (st != FLINT_MOE_OK) return st;
-  return FLINT_MOE_ERR_UNSUPPORTED;
+  if (dims->weight_dtype != FLINT_MOE_W_NVFP4) return FLINT_MOE_ERR_UNSUPPORTED;
+  if ((st = check_layer(dims, layer)) != FLINT_MOE_OK) return st;
+  if (T < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (T > PREFILL_MAX_TOKENS) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (x == nullptr || y == nullptr || ws == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  if (ws_bytes < prefill_ws_bytes(T)) return FLINT_MOE_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+  return to_status(launch_prefill(layer_args(*layer), x, T, dims->rms_eps, y, topk_ids, topk_w, ws, ds->sm_count,
+                                  ds->err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int flint_moe_release(void) {

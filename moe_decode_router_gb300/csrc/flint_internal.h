@@ -43,6 +43,13 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
 
 cudaError_t decode_kernels_init(int device);
 
+// Prefill-shaped sublayer over T tokens (NVFP4 weights): workspace size and
+// the enqueue of its kernels on `st`.
+size_t prefill_ws_bytes(int T);
+cudaError_t prefill_kernels_init(int device);
+cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
+                           float* w_out, void* ws, int sm_count, unsigned* err, cudaStream_t st);
+
 cudaError_t launch_pack(int fmt, const void* gate_up, const uint8_t* gu_scales, const void* down,
                         const uint8_t* dn_scales, void* packed, cudaStream_t st);
 

@@ -1,0 +1,791 @@
+// Prefill-shaped MoE sublayer (T tokens, e.g. 8,192), sm_103a.
+//
+// "Day-0 Support for Flint on vLLM", section "Optimizations": the small-batch
+// MoE kernels also gave the largest gain in the 8,192-token prefill, and the
+// dense kernels run on the same packed NVFP4 weights as the large ones.  Here
+// the sublayer over many tokens is one dense grouped contraction per expert,
+// run on the 5th-generation tensor cores:
+//
+//   prep            per token: optional RMSNorm (exact), x_hat * 2^e in f16
+//                   with a per-token power-of-two e, and an upper bound on
+//                   ||x_hat||_2
+//   router_approx   fp32 logits S[t][e] by plain fused multiply-adds on CUDA
+//                   cores (sequential over K, so |S - exact| <= gamma_2048 *
+//                   ||x_hat|| * ||W_e|| by the IEEE error bound and
+//                   Cauchy-Schwarz)
+//   route           per token, one warp: the experts whose bound interval can
+//                   reach the 6th largest lower bound are recomputed with an
+//                   error-free sum (TwoSum), every other logit is provably
+//                   below the 6th; the top-6 then follows the decode path's
+//                   sigmoid top-6 on the exact bf16 logits
+//   plan, scatter   tokens bucketed by expert (routed experts, then the shared
+//                   expert over all tokens), tile counts per expert
+//   gemm<gate/up>   tcgen05.mma kind::f16 (M=128 weight rows, N=256 tokens,
+//                   fp32 accumulator in tensor memory); NVFP4 weights
+//                   dequantised to f16 (exact) into 128-byte-swizzled shared
+//                   memory, token rows gathered with cp.async; epilogue
+//                   h = bf16(silu(g) * u)
+//   gemm<down>      the same with bf16 operands (h is bf16); epilogue adds
+//                   w_pair * d into an fp32 accumulator (shared expert w = 1)
+//   finalize        y = bf16(accumulator)
+#include "flint_common.cuh"
+#include "flint_internal.h"
+#include "tc05.cuh"
+
+namespace flint {
+
+namespace {
+
+constexpr int PG_M = 128;  // weight rows per tile
+constexpr int PG_N = 256;  // tokens per tile
+constexpr int PG_KS = 64;  // K per pipeline step (one 128-byte swizzle row)
+constexpr int PG_STAGES = 3;
+constexpr int PG_RAW = 2;  // packed-weight K-slices in flight
+constexpr int PG_THREADS = 256;
+constexpr int PG_A_BYTES = PG_M * PG_KS * 2;    // 16 KB
+constexpr int PG_B_BYTES = PG_N * PG_KS * 2;    // 32 KB
+constexpr int PG_RAW_BYTES = 8 * F4_SLICE;      // 8 packed 16-row tiles, one 256-wide K slice
+constexpr float GAMMA_K = 1.2300e-4f;           // >= gamma_2048 = 2048 u / (1 - 2048 u), u = 2^-24
+
+__device__ __forceinline__ float exp2i_p(int e) { return __int_as_float((127 + e) << 23); }
+
+__device__ __forceinline__ int f16_exp_of(float m) {
+  if (!(m > 0.f) || !(m < INFINITY)) return 0;
+  int e = ((__float_as_uint(m) >> 23) & 0xFF) - 127;
+  if (e < -126) e = -126;
+  int s = 14 - e;
+  if (s > 126) s = 126;
+  if (s < -126) s = -126;
+  return s;
+}
+
+__device__ __forceinline__ void bf16x8_f32(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// ---------------------------------------------------------------- prep
+// One CTA (256 threads, 8 columns each) per token.
+__global__ void __launch_bounds__(256) prefill_prep_kernel(const __nv_bfloat16* __restrict__ x,
+                                                           const __nv_bfloat16* __restrict__ norm_w, float eps,
+                                                           __nv_bfloat16* __restrict__ xh, __half* __restrict__ xh16,
+                                                           int* __restrict__ xexp, float* __restrict__ xnorm) {
+  __shared__ CSum red[8];
+  __shared__ float redf[8];
+  __shared__ unsigned redm[8];
+  __shared__ float rs;
+  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int k0 = tid * 8;
+  float v[8];
+  bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + k0)), v);
+  if (norm_w != nullptr) {
+    float w[8];
+    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(norm_w + k0)), w);
+    CSum a = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(v[i], v[i]));
+    a = cs_warp_reduce(a);
+    if (lane == 0) red[warp] = a;
+    __syncthreads();
+    if (tid == 0) {
+      CSum b = red[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) cs_merge(b, red[i]);
+      const float ms = __fmul_rn(cs_value(b), 1.0f / (float)H);
+      rs = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+    }
+    __syncthreads();
+    const float r = rs;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(v[i], r), w[i])));
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) pk[i] = (__float_as_uint(v[2 * i]) >> 16) | (__float_as_uint(v[2 * i + 1]) & 0xFFFF0000u);
+    *reinterpret_cast<uint4*>(xh + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+  float sq = 0.f, m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    sq = fmaf(v[i], v[i], sq);
+    m = fmaxf(m, fabsf(v[i]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+  const unsigned mb = redux_max(__float_as_uint(m));
+  if (lane == 0) {
+    redf[warp] = sq;
+    redm[warp] = mb;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    unsigned mm = 0u;
+    for (int i = 0; i < 8; ++i) {
+      s += redf[i];
+      mm = max(mm, redm[i]);
+    }
+    // upper bound: the fp32 sum of 2048 squares is within 1e-3 (relative) of the exact one
+    xnorm[t] = sqrtf(s) * 1.001f;
+    const int e = f16_exp_of(__uint_as_float(mm));
+    xexp[t] = e;
+    redm[0] = (unsigned)(e + 1000);
+  }
+  __syncthreads();
+  const float sc = exp2i_p((int)redm[0] - 1000);
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 hv = __floats2half2_rn(__fmul_rn(v[2 * i], sc), __fmul_rn(v[2 * i + 1], sc));
+    pk[i] = *reinterpret_cast<const uint32_t*>(&hv);
+  }
+  *reinterpret_cast<uint4*>(xh16 + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+}
+
+// Upper bound on ||W_r[e]||_2, one warp per expert.
+__global__ void __launch_bounds__(256) prefill_wnorm_kernel(const __nv_bfloat16* __restrict__ wr, float* __restrict__ wnorm) {
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[8];
+    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane + 32 * j), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = fmaf(f[i], f[i], s);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) wnorm[e] = sqrtf(s) * 1.001f;
+}
+
+// ---------------------------------------------------------------- router_approx
+// S[t][e] = fp32 sequential fused multiply-add of x_hat[t][k] * W_r[e][k] over
+// k = 0..2047.  CTA tile 128 tokens x 64 experts; thread (ty, tx) owns tokens
+// 8ty..8ty+7 (as 4 packed pairs) and experts 4tx..4tx+3.
+constexpr int RA_TT = 128, RA_TE = 64, RA_KC = 32;
+__global__ void __launch_bounds__(256) prefill_router_approx_kernel(const __nv_bfloat16* __restrict__ xh,
+                                                                    const __nv_bfloat16* __restrict__ wr, int T,
+                                                                    float* __restrict__ S) {
+  __shared__ __align__(16) float xs[RA_KC][RA_TT];      // [k][token]
+  __shared__ __align__(16) float ws[RA_KC][RA_TE * 2];  // [k][expert] duplicated (w, w)
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * RA_TT, e0 = blockIdx.y * RA_TE;
+  uint64_t acc[4][4];  // [token pair][expert]
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0ull;
+  for (int kc = 0; kc < H; kc += RA_KC) {
+    __syncthreads();
+    // x tile: 128 tokens x 32 k = 512 chunks of 8
+    for (int c = tid; c < RA_TT * (RA_KC / 8); c += 256) {
+      const int tt = c >> 2, kk = (c & 3) * 8;
+      const int t = t0 + tt;
+      float f[8];
+      if (t < T) bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(xh + (size_t)t * H + kc + kk)), f);
+      else
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[kk + i][tt] = f[i];
+    }
+    for (int c = tid; c < RA_TE * (RA_KC / 8); c += 256) {
+      const int ee = c >> 2, kk = (c & 3) * 8;
+      float f[8];
+      bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + ee) * H + kc + kk)), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ws[kk + i][2 * ee] = f[i];
+        ws[kk + i][2 * ee + 1] = f[i];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < RA_KC; ++k) {
+      const ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(&xs[k][ty * 8]);
+      const ulonglong2 xb = *reinterpret_cast<const ulonglong2*>(&xs[k][ty * 8 + 4]);
+      const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(&ws[k][tx * 8]);
+      const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(&ws[k][tx * 8 + 4]);
+      const uint64_t xp[4] = {xa.x, xa.y, xb.x, xb.y};
+      const uint64_t wp[4] = {wa.x, wa.y, wb.x, wb.y};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint64_t d;
+          asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(xp[a]), "l"(wp[b]), "l"(acc[a][b]));
+          acc[a][b] = d;
+        }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float lo, hi;
+      f2unpack(acc[a][b], lo, hi);
+      const int t = t0 + ty * 8 + 2 * a, e = e0 + tx * 4 + b;
+      if (t < T) S[(size_t)t * E + e] = lo;
+      if (t + 1 < T) S[(size_t)(t + 1) * E + e] = hi;
+    }
+}
+
+// ---------------------------------------------------------------- route
+// One warp per token.  Lane l holds experts 8l..8l+7.
+__device__ __forceinline__ uint32_t ord_f32(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(256) prefill_route_kernel(
+    const __nv_bfloat16* __restrict__ xh, const __nv_bfloat16* __restrict__ wr, const float* __restrict__ S,
+    const float* __restrict__ xnorm, const float* __restrict__ wnorm, int T, int32_t* __restrict__ ids,
+    float* __restrict__ wts, int* __restrict__ counts, int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
+  __shared__ __align__(16) __nv_bfloat16 lrow[8][E];
+  __shared__ int sids[8][TOPK];
+  __shared__ float sw[8][TOPK];
+  __shared__ uint32_t umask_dummy[8][8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float xn = xnorm[t];
+  float sv[8], eps[8];
+  {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(S + (size_t)t * E + lane * 8));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(S + (size_t)t * E + lane * 8 + 4));
+    const float4 na = __ldg(reinterpret_cast<const float4*>(wnorm + lane * 8));
+    const float4 nb = __ldg(reinterpret_cast<const float4*>(wnorm + lane * 8 + 4));
+    const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const float n8[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sv[i] = s8[i];
+      eps[i] = GAMMA_K * xn * n8[i] * 1.01f;
+    }
+  }
+  // L = 6th largest lower bound (S - eps); ties irrelevant for a bound
+  uint32_t taken = 0u;
+  float L = 0.f;
+  for (int k = 0; k < TOPK; ++k) {
+    uint32_t best = 0u;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t o = ord_f32(sv[i] - eps[i]);
+      if (!((taken >> i) & 1u) && (bi < 0 || o > best)) {
+        best = o;
+        bi = i;
+      }
+    }
+    const uint32_t m = redux_max(best);
+    const unsigned owner = __ballot_sync(0xffffffffu, best == m);
+    const int ol = __ffs(owner) - 1;
+    const int oi = __shfl_sync(0xffffffffu, bi, ol);
+    if (lane == ol) taken |= 1u << oi;
+    const uint32_t fb = (m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m;
+    L = __uint_as_float(fb);
+  }
+  // An expert can be selected only if its bf16 logit reaches bf16(L), so its
+  // exact logit lies within 1.5 bf16 ulps of L (half an ulp either side of the
+  // rounded value, the lower side possibly in the next binade); 2 ulps are kept.
+  const float aL = fabsf(L);
+  const float ulp = aL > 0.f ? __int_as_float(((int)((__float_as_uint(aL) >> 23) & 0xFF) - 7) << 23) : 0.f;
+  const float thr = L - 2.0f * ulp;
+  uint32_t cand = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (sv[i] + eps[i] >= thr) cand |= 1u << i;
+  int total = __popc(cand);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+  // Outside the band where distinct bf16 logits give distinct fp32 scores, or with
+  // too many candidates, every logit is computed exactly.
+  const bool all = total > 32 || !(L > -80.f && L < 8.f) || fabsf(L) < 4.8828125e-4f;
+  if (all) cand = 0xFFu;
+  // x_hat row in registers: 64 elements per lane (lane owns columns 64l..64l+63 as 8 chunks of 8)
+  float xr[64];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[8];
+    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(xh + (size_t)t * H) + lane * 8 + j), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xr[j * 8 + i] = f[i];
+  }
+  for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
+  __syncwarp();
+  // exact logits of the candidates, one expert at a time across the warp
+  for (int src = 0; src < 32; ++src) {
+    const uint32_t cm = __shfl_sync(0xffffffffu, cand, src);
+    for (uint32_t mm = cm; mm; mm &= mm - 1) {
+      const int e = src * 8 + __ffs(mm) - 1;
+      CSum a = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
+      }
+      a = cs_warp_reduce(a);
+      if (lane == 0) lrow[warp][e] = __float2bfloat16_rn(cs_value(a));
+    }
+  }
+  __syncwarp();
+  if (lane < 8) umask_dummy[warp][lane] = 0u;
+  __syncwarp();
+  const uint4 raw = *reinterpret_cast<const uint4*>(&lrow[warp][lane * 8]);
+  warp_topk(raw, lane, sids[warp], sw[warp], umask_dummy[warp]);
+  __syncwarp();
+  if (lane < TOPK) {
+    const int e = sids[warp][lane];
+    const float w = sw[warp][lane];
+    ids[(size_t)t * TOPK + lane] = e;
+    wts[(size_t)t * TOPK + lane] = w;
+    if (ids_out) ids_out[(size_t)t * TOPK + lane] = e;
+    if (w_out) w_out[(size_t)t * TOPK + lane] = w;
+    atomicAdd(&counts[e], 1);
+  }
+}
+
+// ---------------------------------------------------------------- plan, scatter
+// offsets[e]: start of expert e's pairs (experts 0..255 routed, 256 shared);
+// prefix[kind][e]: first work item of expert e (items = tiles of 256 pairs x
+// weight-row tiles of 128).  One CTA.
+__global__ void __launch_bounds__(32 * 9) prefill_plan_kernel(const int* __restrict__ counts, int T,
+                                                              int* __restrict__ offsets, int* __restrict__ gu_prefix,
+                                                              int* __restrict__ dn_prefix) {
+  __shared__ int c[NE];
+  for (int e = threadIdx.x; e < NE; e += blockDim.x) c[e] = e < E ? counts[e] : T;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0, gu = 0, dn = 0;
+    for (int e = 0; e < NE; ++e) {
+      offsets[e] = off;
+      gu_prefix[e] = gu;
+      dn_prefix[e] = dn;
+      const int nt = (c[e] + PG_N - 1) / PG_N;
+      off += c[e];
+      gu += nt * (2 * I / PG_M);
+      dn += nt * (H / PG_M);
+    }
+    offsets[NE] = off;
+    gu_prefix[NE] = gu;
+    dn_prefix[NE] = dn;
+  }
+}
+
+__global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __restrict__ ids,
+                                                              const float* __restrict__ wts,
+                                                              const int* __restrict__ offsets, int* __restrict__ cursor,
+                                                              int T, int* __restrict__ pair_token,
+                                                              float* __restrict__ pair_w) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q < T * TOPK) {
+    const int t = q / TOPK, e = ids[q];
+    const int pos = offsets[e] + atomicAdd(&cursor[e], 1);
+    pair_token[pos] = t;
+    pair_w[pos] = wts[q];
+  } else if (q < T * (TOPK + 1)) {
+    const int t = q - T * TOPK;
+    pair_token[offsets[E] + t] = t;
+    pair_w[offsets[E] + t] = 1.0f;
+  }
+}
+
+// ---------------------------------------------------------------- grouped GEMM
+struct GemmParams {
+  const uint8_t* experts;
+  const float* tscale;     // [NE][2]
+  const int* prefix;       // [NE + 1] first item of each expert
+  const int* offsets;      // [NE + 1]
+  const int* pair_token;   // [P]
+  const float* pair_w;     // [P]
+  const uint16_t* bsrc;    // gate/up: x_hat f16 [T][H]; down: h bf16 [P][I]
+  const int* xexp;         // [T]
+  uint16_t* h;             // gate/up output [P][I]
+  float* yacc;             // down output [T][H]
+  unsigned* err;
+};
+
+template <int KIND>
+struct GemmCfg {
+  static constexpr int K = KIND == 0 ? H : I;
+  static constexpr int NKS = K / PG_KS;
+  static constexpr int MT = (KIND == 0 ? 2 * I : H) / PG_M;
+  static constexpr int TILE = KIND == 0 ? F4_GU_TILE : F4_DN_TILE;
+  static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
+  static constexpr uint32_t IDESC = tc05::idesc_f16(PG_M, PG_N, KIND == 0 ? 0 : 1);
+};
+
+constexpr size_t PG_SMEM = 1024 + (size_t)PG_STAGES * (PG_A_BYTES + PG_B_BYTES) + (size_t)PG_RAW * PG_RAW_BYTES + 1024 +
+                           3 * PG_N * 4 + 2 * (NE + 1) * 4;
+
+// f16 (KIND 0) or bf16 (KIND 1) pair of dequantised weights from one E2M1 byte and a scale.
+template <int KIND>
+__device__ __forceinline__ uint32_t dq_pair(uint32_t f16pair, uint32_t scale16x2_lohalf, float scale_f) {
+  if (KIND == 0) return hmul2_lo(f16pair, scale16x2_lohalf);
+  const __half2 hv = *reinterpret_cast<const __half2*>(&f16pair);
+  const float2 f = __half22float2(hv);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(f.x, scale_f), __fmul_rn(f.y, scale_f));
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(PG_THREADS, 1) prefill_gemm_kernel(const GemmParams p) {
+  using C = GemmCfg<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stA = sm;                                               // [STAGES][A]
+  uint8_t* stB = sm + PG_STAGES * PG_A_BYTES;                      // [STAGES][B]
+  uint8_t* raw = stB + PG_STAGES * PG_B_BYTES;                     // [RAW][8][2304]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + PG_RAW * PG_RAW_BYTES);  // raw_full[2], mma[3]
+  uint64_t* raw_full = bars;
+  uint64_t* mma_bar = bars + PG_RAW;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+  int* rowsrc = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 1024);
+  float* colf = reinterpret_cast<float*>(rowsrc + PG_N);  // gate/up: 2^-xexp ; down: pair weight
+  int* coltok = reinterpret_cast<int*>(colf + PG_N);
+  int* sprefix = coltok + PG_N;   // [NE + 1]
+  int* soffs = sprefix + NE + 1;  // [NE + 1]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e <= NE; e += PG_THREADS) {
+    sprefix[e] = p.prefix[e];
+    soffs[e] = p.offsets[e];
+  }
+  if (warp == 0) {
+    tc05::tmem_alloc(tslot, PG_N);
+    tc05::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < PG_RAW; ++i) mbar_init(&raw_full[i], 1);
+    for (int i = 0; i < PG_STAGES; ++i) mbar_init(&mma_bar[i], 1);
+    fence_mbar_init();
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  tc05::fence_after_sync();
+  const uint32_t tmem = *tslot;
+  const int n_items = sprefix[NE];
+  // Ring positions carried across items: MMA steps and packed-weight slices
+  // issued by this CTA before the current item.  Step g uses operand stage
+  // g % PG_STAGES and is the (g / PG_STAGES)-th commit on that stage's
+  // barrier; slice g uses slot g % PG_RAW likewise.
+  uint32_t mma_base = 0, raw_base = 0, raw_issued = 0;
+  bool failed = false;
+
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // ---- decode the item: expert, token tile, weight-row tile
+    int lo = 0, hi = NE;  // largest e with sprefix[e] <= item
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sprefix[mid] <= item) lo = mid;
+      else hi = mid;
+    }
+    const int e = lo;
+    const int local = item - sprefix[e];
+    const int mtile = local % C::MT, ntile = local / C::MT;
+    const int pair0 = soffs[e] + ntile * PG_N;
+    const int nvalid = min(PG_N, soffs[e + 1] - pair0);
+    {
+      const int r = tid;  // PG_THREADS == PG_N
+      const int pr = pair0 + min(r, nvalid - 1);
+      const int tok = p.pair_token[pr];
+      coltok[r] = tok;
+      if (KIND == 0) {
+        rowsrc[r] = tok;
+        colf[r] = exp2i_p(-p.xexp[tok]);
+      } else {
+        rowsrc[r] = pr;
+        colf[r] = p.pair_w[pr];
+      }
+    }
+    __syncthreads();
+    const uint8_t* wbase = p.experts + (size_t)e * F4_EXPERT + C::BASE + (size_t)mtile * 8 * C::TILE;
+    auto issue_raw = [&](int q) {  // one 256-wide K slice of the 8 row tiles (thread 0)
+      const uint32_t slot = (raw_base + (uint32_t)q) % PG_RAW;
+      mbar_arrive_expect_tx(&raw_full[slot], PG_RAW_BYTES);
+      const uint64_t pol = l2_evict_first();
+      for (int r = 0; r < 8; ++r)
+        bulk_g2s(raw + slot * PG_RAW_BYTES + r * F4_SLICE, wbase + (size_t)r * C::TILE + (size_t)q * F4_SLICE,
+                 F4_SLICE, &raw_full[slot], pol);
+      ++raw_issued;
+    };
+    auto stage_of = [&](int ks) { return (int)((mma_base + (uint32_t)ks) % PG_STAGES); };
+    auto issue_b = [&](int ks) {  // 256 token rows x 64 K, row = thread
+      uint8_t* dst = stB + stage_of(ks) * PG_B_BYTES;
+      const uint16_t* src = p.bsrc + (size_t)rowsrc[tid] * C::K + ks * PG_KS;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) cp_async16(dst + tc05::sw128_off(tid, ch * 8), src + ch * 8);
+    };
+    auto wait_mma = [&](int ks) {  // MMA step ks of this item has completed
+      const uint32_t gs = mma_base + (uint32_t)ks;
+      if (!failed && !mbar_wait(&mma_bar[gs % PG_STAGES], (gs / PG_STAGES) & 1)) {
+        atomicOr(p.err, ERR_WAIT_FULL);
+        failed = true;
+      }
+    };
+    constexpr int NQ = C::NKS / 4;
+    if (tid == 0) {
+      issue_raw(0);
+      if (NQ > 1) issue_raw(1);
+    }
+    issue_b(0);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (C::NKS > 1) issue_b(1);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+
+    for (int ks = 0; ks < C::NKS; ++ks) {
+      const int s = stage_of(ks), q = ks / 4, c4 = ks % 4;
+      const uint32_t gq = raw_base + (uint32_t)q;
+      if (c4 == 0 && !failed && !mbar_wait(&raw_full[gq % PG_RAW], (gq / PG_RAW) & 1)) {
+        atomicOr(p.err, ERR_WAIT_FULL);
+        failed = true;
+      }
+      // ---- A: dequantise chunk c4 of slice q for the 8 row tiles (warp = row tile)
+      {
+        const uint8_t* sl = raw + (gq % PG_RAW) * PG_RAW_BYTES + warp * F4_SLICE;
+        const uint4 cw = *reinterpret_cast<const uint4*>(sl + c4 * 512 + lane * 16);
+        const int g = lane >> 2, t = lane & 3;
+        const uint2 sc8 = *reinterpret_cast<const uint2*>(sl + F4_CODES + (c4 >> 1) * 128 + g * 16 + 8 * (c4 & 1));
+        const uint32_t scw[2] = {sc8.x, sc8.y};
+        const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+        uint8_t* At = stA + s * PG_A_BYTES;
+        const int rg = warp * 16 + g, rg8 = rg + 8;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t pair16 = (scw[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+          const uint32_t sc = e4m3x2_to_f16x2(pair16);
+          float sg = 0.f, sg8 = 0.f;
+          if (KIND == 1) {
+            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
+            sg = sf.x;
+            sg8 = sf.y;
+          }
+          uint32_t a0, a1, a2, a3;
+          e2m1x8_to_f16x2(w4[j], a0, a1, a2, a3);
+          const uint32_t hi_sc = __byte_perm(sc, 0, 0x3232);
+          const uint32_t v0 = dq_pair<KIND>(a0, sc, sg);       // row g,   k 16j+2t
+          const uint32_t v1 = dq_pair<KIND>(a1, hi_sc, sg8);   // row g+8, k 16j+2t
+          const uint32_t v2 = dq_pair<KIND>(a2, sc, sg);       // row g,   k 16j+2t+8
+          const uint32_t v3 = dq_pair<KIND>(a3, hi_sc, sg8);   // row g+8, k 16j+2t+8
+          const int k = 16 * j + 2 * t;
+          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg, k)) = v0;
+          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg8, k)) = v1;
+          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg, k + 8)) = v2;
+          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg8, k + 8)) = v3;
+        }
+      }
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      tc05::fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tc05::fence_after_sync();
+        if (c4 == 3 && q + PG_RAW < NQ) issue_raw(q + PG_RAW);  // every thread is past slice q
+        const uint64_t da = tc05::sw128_desc(smem_u32(stA + s * PG_A_BYTES));
+        const uint64_t db = tc05::sw128_desc(smem_u32(stB + s * PG_B_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc05::mma_f16(tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), C::IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+        tc05::commit(&mma_bar[s]);
+      }
+      // the stage of step ks + 2 was last read by MMA step ks - 1 (or by an
+      // earlier item, whose last step was waited for before its epilogue)
+      if (ks + 2 < C::NKS) {
+        if (ks >= 1) wait_mma(ks - 1);
+        issue_b(ks + 2);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    wait_mma(C::NKS - 1);
+    mma_base += C::NKS;
+    raw_base += NQ;
+    tc05::fence_after_sync();
+
+    // ---- epilogue: warp w reads TMEM lanes 32(w%4).., columns [128(w/4), +128)
+    const int sub = warp & 3, half = warp >> 2;
+    const int m = sub * 32 + lane;  // weight row within the tile
+    const float ts = __ldg(p.tscale + 2 * e + KIND);
+    for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
+      uint32_t v[32];
+      tc05::ld_32x32b_x32(tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)c0, v);
+      tc05::wait_ld();
+      if (KIND == 0) {
+        const int tr = m & 15;
+        const int j = (mtile * 8 + (m >> 4)) * 8 + (tr & 7);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float mine = __uint_as_float(v[c]);
+          const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
+          const int col = c0 + c;
+          if (tr < 8 && col < nvalid) {
+            const float f = __fmul_rn(ts, colf[col]);
+            const float gate = __fmul_rn(mine, f);
+            const float up = __fmul_rn(other, f);
+            const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
+            const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
+            p.h[(size_t)(pair0 + col) * I + j] = *reinterpret_cast<const uint16_t*>(&hv);
+          }
+        }
+      } else {
+        const int orow = mtile * PG_M + m;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = c0 + c;
+          if (col < nvalid) {
+            const float d = __fmul_rn(__uint_as_float(v[c]), ts);
+            atomicAdd(p.yacc + (size_t)coltok[col] * H + orow, __fmul_rn(colf[col], d));
+          }
+        }
+      }
+    }
+    tc05::fence_before_sync();
+    failed = __syncthreads_or(failed ? 1 : 0) != 0;
+    tc05::fence_after_sync();
+    if (failed) break;
+  }
+  if (failed && tid == 0) {
+    // A wait ran out: let the copies and MMAs this CTA issued finish (each
+    // wait again bounded) before the shared and tensor memory are released.
+    for (uint32_t g = raw_issued > PG_RAW ? raw_issued - PG_RAW : 0; g < raw_issued; ++g)
+      (void)mbar_wait(&raw_full[g % PG_RAW], (g / PG_RAW) & 1);
+    if (mma_base > 0) (void)mbar_wait(&mma_bar[(mma_base - 1) % PG_STAGES], ((mma_base - 1) / PG_STAGES) & 1);
+    atomicOr(p.err, ERR_DRAIN);
+  }
+  tc05::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc05::fence_after_sync();
+    tc05::tmem_dealloc(tmem, PG_N);
+  }
+}
+
+__global__ void prefill_finalize_kernel(const float4* __restrict__ yacc, uint2* __restrict__ y, size_t n4) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = yacc[i];
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  y[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
+size_t a256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+// ---------------------------------------------------------------- workspace and launch
+
+struct PrefillWs {
+  __nv_bfloat16* xh;  // [T][H] (only with a norm)
+  __half* xh16;       // [T][H]
+  int* xexp;          // [T]
+  float* xnorm;       // [T]
+  float* wnorm;       // [E]
+  float* S;           // [T][E]
+  int32_t* ids;       // [T][6]
+  float* wts;         // [T][6]
+  int* counts;        // [E]
+  int* cursor;        // [E]
+  int* offsets;       // [NE + 1]
+  int* gu_prefix;     // [NE + 1]
+  int* dn_prefix;     // [NE + 1]
+  int* pair_token;    // [7T]
+  float* pair_w;      // [7T]
+  uint16_t* h;        // [7T][I]
+  float* yacc;        // [T][H]
+};
+
+static PrefillWs carve_prefill(void* ws, int T, size_t* total) {
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += a256(bytes);
+    return r;
+  };
+  PrefillWs w;
+  const size_t P = (size_t)T * (TOPK + 1);
+  w.xh = reinterpret_cast<__nv_bfloat16*>(take((size_t)T * H * 2));
+  w.xh16 = reinterpret_cast<__half*>(take((size_t)T * H * 2));
+  w.xexp = reinterpret_cast<int*>(take((size_t)T * 4));
+  w.xnorm = reinterpret_cast<float*>(take((size_t)T * 4));
+  w.wnorm = reinterpret_cast<float*>(take((size_t)E * 4));
+  w.S = reinterpret_cast<float*>(take((size_t)T * E * 4));
+  w.ids = reinterpret_cast<int32_t*>(take((size_t)T * TOPK * 4));
+  w.wts = reinterpret_cast<float*>(take((size_t)T * TOPK * 4));
+  w.counts = reinterpret_cast<int*>(take((size_t)E * 4));
+  w.cursor = reinterpret_cast<int*>(take((size_t)E * 4));
+  w.offsets = reinterpret_cast<int*>(take((size_t)(NE + 1) * 4));
+  w.gu_prefix = reinterpret_cast<int*>(take((size_t)(NE + 1) * 4));
+  w.dn_prefix = reinterpret_cast<int*>(take((size_t)(NE + 1) * 4));
+  w.pair_token = reinterpret_cast<int*>(take(P * 4));
+  w.pair_w = reinterpret_cast<float*>(take(P * 4));
+  w.h = reinterpret_cast<uint16_t*>(take(P * I * 2));
+  w.yacc = reinterpret_cast<float*>(take((size_t)T * H * 4));
+  if (total) *total = off;
+  return w;
+}
+
+size_t prefill_ws_bytes(int T) {
+  size_t total = 0;
+  carve_prefill(nullptr, T, &total);
+  return total;
+}
+
+cudaError_t prefill_kernels_init(int /*device*/) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PG_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PG_SMEM);
+}
+
+cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
+                           float* w_out, void* ws, int sm_count, unsigned* err, cudaStream_t st) {
+  PrefillWs w = carve_prefill(ws, T, nullptr);
+  const __nv_bfloat16* xin = static_cast<const __nv_bfloat16*>(x);
+  const __nv_bfloat16* norm = static_cast<const __nv_bfloat16*>(L.norm_w);
+  const __nv_bfloat16* xh = norm ? w.xh : xin;
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(w.counts, 0, E * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(w.cursor, 0, E * 4, st)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(w.yacc, 0, (size_t)T * H * 4, st)) != cudaSuccess) return e;
+  prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm);
+  prefill_wnorm_kernel<<<E / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(L.router_w), w.wnorm);
+  prefill_router_approx_kernel<<<dim3((T + RA_TT - 1) / RA_TT, E / RA_TE), 256, 0, st>>>(
+      xh, static_cast<const __nv_bfloat16*>(L.router_w), T, w.S);
+  prefill_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(xh, static_cast<const __nv_bfloat16*>(L.router_w), w.S, w.xnorm,
+                                                    w.wnorm, T, w.ids, w.wts, w.counts, ids_out, w_out);
+  prefill_plan_kernel<<<1, 32 * 9, 0, st>>>(w.counts, T, w.offsets, w.gu_prefix, w.dn_prefix);
+  const int nq = T * (TOPK + 1);
+  prefill_scatter_kernel<<<(nq + 255) / 256, 256, 0, st>>>(w.ids, w.wts, w.offsets, w.cursor, T, w.pair_token,
+                                                            w.pair_w);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  GemmParams gp;
+  gp.experts = L.experts;
+  gp.tscale = L.tscale;
+  gp.offsets = w.offsets;
+  gp.pair_token = w.pair_token;
+  gp.pair_w = w.pair_w;
+  gp.xexp = w.xexp;
+  gp.h = w.h;
+  gp.yacc = w.yacc;
+  gp.err = err;
+  gp.prefix = w.gu_prefix;
+  gp.bsrc = reinterpret_cast<const uint16_t*>(w.xh16);
+  prefill_gemm_kernel<0><<<sm_count, PG_THREADS, PG_SMEM, st>>>(gp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  gp.prefix = w.dn_prefix;
+  gp.bsrc = w.h;
+  prefill_gemm_kernel<1><<<sm_count, PG_THREADS, PG_SMEM, st>>>(gp);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t n4 = (size_t)T * H / 4;
+  prefill_finalize_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4*>(w.yacc),
+                                                                       static_cast<uint2*>(y), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace flint

@@ -111,3 +111,23 @@ def test_status_strings(lib):
     for st in (0, -1, -2, -3, -4, -5):
         assert lib.flint_moe_status_string(st)
     assert lib.flint_moe_status_string(-99) == b"unknown status"
+
+
+def test_prefill_rejects_bad_arguments_on_host(lib):
+    d = F.dims()
+    ws_b = F.workspace_bytes(F.W_NVFP4, 8192)
+    assert ws_b >= F.workspace_bytes(F.W_NVFP4, 8) and ws_b % 256 == 0
+    assert F.workspace_bytes(F.W_BF16, 9) == 0  # prefill takes NVFP4 weights only
+
+    def call(dd=None, T=8192, x=FAKE + 1024, y=FAKE + 2048, ws=FAKE + 4096, n=ws_b, L=None):
+        return lib.flint_moe_prefill_layer(ctypes.byref(dd or d), ctypes.byref(L or _layer()), x, T, y, None,
+                                           None, ws, n, None)
+
+    assert call(T=0) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert call(T=(1 << 20) + 1) == F.FLINT_MOE_ERR_UNSUPPORTED
+    assert call(dd=F.dims(F.W_BF16)) == F.FLINT_MOE_ERR_UNSUPPORTED
+    assert call(n=ws_b - 256) == F.FLINT_MOE_ERR_WORKSPACE
+    assert call(y=FAKE + 1024) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert call(x=FAKE + 1032) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert call(ws=FAKE + 4112) == F.FLINT_MOE_ERR_INVALID_ARG
+    assert call(L=_layer(tensor_scales=None)) == F.FLINT_MOE_ERR_INVALID_ARG
