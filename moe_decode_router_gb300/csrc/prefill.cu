@@ -39,12 +39,6 @@ namespace {
 constexpr int PG_M = 128;  // weight rows per tile
 constexpr int PG_N = 256;  // tokens per tile
 constexpr int PG_KS = 64;  // K per pipeline step (one 128-byte swizzle row)
-constexpr int PG_STAGES = 3;
-constexpr int PG_RAW = 2;  // packed-weight K-slices in flight
-constexpr int PG_THREADS = 256;
-constexpr int PG_A_BYTES = PG_M * PG_KS * 2;    // 16 KB
-constexpr int PG_B_BYTES = PG_N * PG_KS * 2;    // 32 KB
-constexpr int PG_RAW_BYTES = 8 * F4_SLICE;      // 8 packed 16-row tiles, one 256-wide K slice
 constexpr float GAMMA_K = 1.2300e-4f;           // >= gamma_2048 = 2048 u / (1 - 2048 u), u = 2^-24
 
 __device__ __forceinline__ float exp2i_p(int e) { return __int_as_float((127 + e) << 23); }
@@ -397,6 +391,28 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 }
 
 // ---------------------------------------------------------------- grouped GEMM
+// One persistent CTA per SM walks work items (expert, token tile, 128-row
+// weight tile), interleaved over CTAs.  Item = D[128 x N] = W[128 x K] *
+// Xg[N x K]^T with N = the tile's token count rounded up to 16, K = 2048
+// (gate/up) or 512 (down), in steps of 64 along K.  Two rings in shared
+// memory: a 4-stage operand ring (dequantised A, gathered B) and a 5-slot
+// ring of raw packed weight bytes.  Warp roles:
+//   warps 0-3   B producers: warp w gathers the N token rows of every step
+//               g = w (mod 4) into operand stage w with cp.async, waits for
+//               its own copies, fences them for the tensor core and signals
+//   warp 4      lane 0 issues the TMA copies of the raw weight bytes of a
+//               step (8 row tiles x (512 code bytes + 256 scale bytes));
+//               the warp owns the tensor-memory allocation
+//   warp 5      lane 0 issues tcgen05.mma (4 per step) into one of two
+//               256-column fp32 accumulators in tensor memory
+//   warps 8-11  epilogue: tensor memory -> registers (lane quadrant = warp
+//               % 4), SiLU*up -> h (gate/up) or weighted add into the fp32
+//               output (down); overlaps the next item's main loop
+//   warps 12-19 dequantisers: warp 12+r turns row tile r of a step into f16
+//               (gate/up) or bf16 (down) with stmatrix into the
+//               128-byte-swizzled A stage
+// Every mbarrier wait is bounded; one that runs out sets the device error
+// word and an abort flag that ends every role's loop.
 struct GemmParams {
   const uint8_t* experts;
   const float* tscale;     // [NE][2]
@@ -418,13 +434,29 @@ struct GemmCfg {
   static constexpr int MT = (KIND == 0 ? 2 * I : H) / PG_M;
   static constexpr int TILE = KIND == 0 ? F4_GU_TILE : F4_DN_TILE;
   static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
-  static constexpr uint32_t IDESC = tc05::idesc_f16(PG_M, PG_N, KIND == 0 ? 0 : 1);
 };
 
-constexpr size_t PG_SMEM = 1024 + (size_t)PG_STAGES * (PG_A_BYTES + PG_B_BYTES) + (size_t)PG_RAW * PG_RAW_BYTES + 1024 +
-                           3 * PG_N * 4 + 2 * (NE + 1) * 4;
+constexpr int GS = 4;                          // operand ring stages (one per B producer warp)
+constexpr int RS = 5;                          // raw weight ring slots
+constexpr int G_THREADS = 640;                 // 20 warps
+constexpr int G_RAW_TILE = 768;                // 512 code bytes + 256 scale bytes of one row tile
+constexpr int G_A = PG_M * PG_KS * 2;          // 16 KB
+constexpr int G_B = PG_N * PG_KS * 2;          // 32 KB
+constexpr int G_STAGE = G_A + G_B;             // 48 KB (1024-byte multiple)
+constexpr int G_RAW = 8 * G_RAW_TILE;          // 6 KB
+static_assert(G_STAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+static_assert((H / PG_KS) % 2 == 0 && (I / PG_KS) % 2 == 0, "dequantisers take two steps per pass");
+constexpr size_t G_SMEM = 1024 + (size_t)GS * G_STAGE + (size_t)RS * G_RAW + 256;
+static_assert(G_SMEM <= 232448, "shared memory per CTA");
 
-// f16 (KIND 0) or bf16 (KIND 1) pair of dequantised weights from one E2M1 byte and a scale.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// f16 (KIND 0) or bf16 (KIND 1) pair of dequantised weights: code pair (f16x2)
+// times the block scale; both results are exact (at most 6 significant bits).
 template <int KIND>
 __device__ __forceinline__ uint32_t dq_pair(uint32_t f16pair, uint32_t scale16x2_lohalf, float scale_f) {
   if (KIND == 0) return hmul2_lo(f16pair, scale16x2_lohalf);
@@ -434,234 +466,327 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t f16pair, uint32_t scale16x2
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
+struct ItemInfo {
+  int e, mtile, pair0, nvalid, n;  // n = MMA width (nvalid rounded up to 16)
+};
+__device__ __forceinline__ ItemInfo decode_item(int item, const int* __restrict__ prefix,
+                                                const int* __restrict__ offs, int MT) {
+  int lo = 0, hi = NE;  // largest e with prefix[e] <= item
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(prefix + mid) <= item) lo = mid;
+    else hi = mid;
+  }
+  ItemInfo it;
+  it.e = lo;
+  const int local = item - __ldg(prefix + lo);
+  it.mtile = local % MT;
+  const int ntile = local / MT;
+  it.pair0 = __ldg(offs + lo) + ntile * PG_N;
+  it.nvalid = min(PG_N, __ldg(offs + lo + 1) - it.pair0);
+  it.n = (it.nvalid + 15) & ~15;
+  return it;
+}
+
 template <int KIND>
-__global__ void __launch_bounds__(PG_THREADS, 1) prefill_gemm_kernel(const GemmParams p) {
+__global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmParams p) {
   using C = GemmCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stA = sm;                                               // [STAGES][A]
-  uint8_t* stB = sm + PG_STAGES * PG_A_BYTES;                      // [STAGES][B]
-  uint8_t* raw = stB + PG_STAGES * PG_B_BYTES;                     // [RAW][8][2304]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(raw + PG_RAW * PG_RAW_BYTES);  // raw_full[2], mma[3]
-  uint64_t* raw_full = bars;
-  uint64_t* mma_bar = bars + PG_RAW;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
-  int* rowsrc = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 1024);
-  float* colf = reinterpret_cast<float*>(rowsrc + PG_N);  // gate/up: 2^-xexp ; down: pair weight
-  int* coltok = reinterpret_cast<int*>(colf + PG_N);
-  int* sprefix = coltok + PG_N;   // [NE + 1]
-  int* soffs = sprefix + NE + 1;  // [NE + 1]
+  uint8_t* rawring = sm + GS * G_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawring + RS * G_RAW);
+  uint64_t* bfull = bars;                  // [GS] B rows landed (32 lanes of the stage's producer warp)
+  uint64_t* afull = bars + GS;             // [GS] A stage written (8 dequant warps)
+  uint64_t* empty = bars + 2 * GS;         // [GS] MMAs of the stage done (tcgen05.commit)
+  uint64_t* rfull = bars + 3 * GS;         // [RS] raw bytes landed (TMA transaction count)
+  uint64_t* rempty = bars + 3 * GS + RS;   // [RS] raw slot read (8 dequant warps)
+  uint64_t* accfull = bars + 3 * GS + 2 * RS;       // [2] accumulator complete (tcgen05.commit)
+  uint64_t* accempty = bars + 3 * GS + 2 * RS + 2;  // [2] accumulator read out (4 epilogue warps)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * GS + 2 * RS + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int e = tid; e <= NE; e += PG_THREADS) {
-    sprefix[e] = p.prefix[e];
-    soffs[e] = p.offsets[e];
-  }
-  if (warp == 0) {
-    tc05::tmem_alloc(tslot, PG_N);
+  if (warp == 4) {
+    tc05::tmem_alloc(tslot, 2 * PG_N);
     tc05::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < PG_RAW; ++i) mbar_init(&raw_full[i], 1);
-    for (int i = 0; i < PG_STAGES; ++i) mbar_init(&mma_bar[i], 1);
+    for (int i = 0; i < GS; ++i) {
+      mbar_init(&bfull[i], 32);
+      mbar_init(&afull[i], 8);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 8);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], 4);
+    }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   tc05::fence_before_sync();
   __syncthreads();
   tc05::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const int n_items = sprefix[NE];
-  // Ring positions carried across items: MMA steps and packed-weight slices
-  // issued by this CTA before the current item.  Step g uses operand stage
-  // g % PG_STAGES and is the (g / PG_STAGES)-th commit on that stage's
-  // barrier; slice g uses slot g % PG_RAW likewise.
-  uint32_t mma_base = 0, raw_base = 0, raw_issued = 0;
-  bool failed = false;
+  const int n_items = __ldg(p.prefix + NE);
+  auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity)) return true;
+    atomicOr(p.err, ERR_WAIT_FULL);
+    *abort_flag = 1;
+    return false;
+  };
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    // ---- decode the item: expert, token tile, weight-row tile
-    int lo = 0, hi = NE;  // largest e with sprefix[e] <= item
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sprefix[mid] <= item) lo = mid;
-      else hi = mid;
-    }
-    const int e = lo;
-    const int local = item - sprefix[e];
-    const int mtile = local % C::MT, ntile = local / C::MT;
-    const int pair0 = soffs[e] + ntile * PG_N;
-    const int nvalid = min(PG_N, soffs[e + 1] - pair0);
-    {
-      const int r = tid;  // PG_THREADS == PG_N
-      const int pr = pair0 + min(r, nvalid - 1);
-      const int tok = p.pair_token[pr];
-      coltok[r] = tok;
-      if (KIND == 0) {
-        rowsrc[r] = tok;
-        colf[r] = exp2i_p(-p.xexp[tok]);
-      } else {
-        rowsrc[r] = pr;
-        colf[r] = p.pair_w[pr];
-      }
-    }
-    __syncthreads();
-    const uint8_t* wbase = p.experts + (size_t)e * F4_EXPERT + C::BASE + (size_t)mtile * 8 * C::TILE;
-    auto issue_raw = [&](int q) {  // one 256-wide K slice of the 8 row tiles (thread 0)
-      const uint32_t slot = (raw_base + (uint32_t)q) % PG_RAW;
-      mbar_arrive_expect_tx(&raw_full[slot], PG_RAW_BYTES);
-      const uint64_t pol = l2_evict_first();
-      for (int r = 0; r < 8; ++r)
-        bulk_g2s(raw + slot * PG_RAW_BYTES + r * F4_SLICE, wbase + (size_t)r * C::TILE + (size_t)q * F4_SLICE,
-                 F4_SLICE, &raw_full[slot], pol);
-      ++raw_issued;
-    };
-    auto stage_of = [&](int ks) { return (int)((mma_base + (uint32_t)ks) % PG_STAGES); };
-    auto issue_b = [&](int ks) {  // 256 token rows x 64 K, row = thread
-      uint8_t* dst = stB + stage_of(ks) * PG_B_BYTES;
-      const uint16_t* src = p.bsrc + (size_t)rowsrc[tid] * C::K + ks * PG_KS;
+  if (warp < 4) {
+    // ---------------- B producers: warp w owns operand stage w (steps g = w mod 4)
+    uint32_t g = 0;  // global step of this CTA
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const uint16_t* src[8];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) cp_async16(dst + tc05::sw128_off(tid, ch * 8), src + ch * 8);
-    };
-    auto wait_mma = [&](int ks) {  // MMA step ks of this item has completed
-      const uint32_t gs = mma_base + (uint32_t)ks;
-      if (!failed && !mbar_wait(&mma_bar[gs % PG_STAGES], (gs / PG_STAGES) & 1)) {
-        atomicOr(p.err, ERR_WAIT_FULL);
-        failed = true;
+      for (int i = 0; i < 8; ++i) {
+        const int r = lane + 32 * i;
+        const int pr = it.pair0 + min(r, it.nvalid - 1);
+        const int row = KIND == 0 ? __ldg(p.pair_token + pr) : pr;
+        src[i] = p.bsrc + (size_t)row * C::K;
       }
-    };
-    constexpr int NQ = C::NKS / 4;
-    if (tid == 0) {
-      issue_raw(0);
-      if (NQ > 1) issue_raw(1);
-    }
-    issue_b(0);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    if (C::NKS > 1) issue_b(1);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-
-    for (int ks = 0; ks < C::NKS; ++ks) {
-      const int s = stage_of(ks), q = ks / 4, c4 = ks % 4;
-      const uint32_t gq = raw_base + (uint32_t)q;
-      if (c4 == 0 && !failed && !mbar_wait(&raw_full[gq % PG_RAW], (gq / PG_RAW) & 1)) {
-        atomicOr(p.err, ERR_WAIT_FULL);
-        failed = true;
-      }
-      // ---- A: dequantise chunk c4 of slice q for the 8 row tiles (warp = row tile)
-      {
-        const uint8_t* sl = raw + (gq % PG_RAW) * PG_RAW_BYTES + warp * F4_SLICE;
-        const uint4 cw = *reinterpret_cast<const uint4*>(sl + c4 * 512 + lane * 16);
-        const int g = lane >> 2, t = lane & 3;
-        const uint2 sc8 = *reinterpret_cast<const uint2*>(sl + F4_CODES + (c4 >> 1) * 128 + g * 16 + 8 * (c4 & 1));
-        const uint32_t scw[2] = {sc8.x, sc8.y};
-        const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
-        uint8_t* At = stA + s * PG_A_BYTES;
-        const int rg = warp * 16 + g, rg8 = rg + 8;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t pair16 = (scw[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-          const uint32_t sc = e4m3x2_to_f16x2(pair16);
-          float sg = 0.f, sg8 = 0.f;
-          if (KIND == 1) {
-            const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
-            sg = sf.x;
-            sg8 = sf.y;
-          }
-          uint32_t a0, a1, a2, a3;
-          e2m1x8_to_f16x2(w4[j], a0, a1, a2, a3);
-          const uint32_t hi_sc = __byte_perm(sc, 0, 0x3232);
-          const uint32_t v0 = dq_pair<KIND>(a0, sc, sg);       // row g,   k 16j+2t
-          const uint32_t v1 = dq_pair<KIND>(a1, hi_sc, sg8);   // row g+8, k 16j+2t
-          const uint32_t v2 = dq_pair<KIND>(a2, sc, sg);       // row g,   k 16j+2t+8
-          const uint32_t v3 = dq_pair<KIND>(a3, hi_sc, sg8);   // row g+8, k 16j+2t+8
-          const int k = 16 * j + 2 * t;
-          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg, k)) = v0;
-          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg8, k)) = v1;
-          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg, k + 8)) = v2;
-          *reinterpret_cast<uint32_t*>(At + tc05::sw128_off(rg8, k + 8)) = v3;
+      for (int ks = 0; ks < C::NKS; ++ks, ++g) {
+        if ((int)(g % GS) != warp) continue;
+        if (!wait(&empty[warp], ((g / GS) & 1) ^ 1)) {
+          ok = false;
+          break;
         }
-      }
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
-      tc05::fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc05::fence_after_sync();
-        if (c4 == 3 && q + PG_RAW < NQ) issue_raw(q + PG_RAW);  // every thread is past slice q
-        const uint64_t da = tc05::sw128_desc(smem_u32(stA + s * PG_A_BYTES));
-        const uint64_t db = tc05::sw128_desc(smem_u32(stB + s * PG_B_BYTES));
+        uint8_t* dst = sm + warp * G_STAGE + G_A;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc05::mma_f16(tmem, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), C::IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
-        tc05::commit(&mma_bar[s]);
+        for (int i = 0; i < 8; ++i) {
+          const int r = lane + 32 * i;
+          if (r < it.n) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) cp_async16(dst + tc05::sw128_off(r, ch * 8), src[i] + ks * PG_KS + ch * 8);
+          }
+        }
+        asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+        tc05::fence_proxy_async_smem();
+        mbar_arrive(&bfull[warp]);
       }
-      // the stage of step ks + 2 was last read by MMA step ks - 1 (or by an
-      // earlier item, whose last step was waited for before its epilogue)
-      if (ks + 2 < C::NKS) {
-        if (ks >= 1) wait_mma(ks - 1);
-        issue_b(ks + 2);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    wait_mma(C::NKS - 1);
-    mma_base += C::NKS;
-    raw_base += NQ;
-    tc05::fence_after_sync();
-
-    // ---- epilogue: warp w reads TMEM lanes 32(w%4).., columns [128(w/4), +128)
-    const int sub = warp & 3, half = warp >> 2;
-    const int m = sub * 32 + lane;  // weight row within the tile
-    const float ts = __ldg(p.tscale + 2 * e + KIND);
-    for (int c0 = half * 128; c0 < half * 128 + 128; c0 += 32) {
-      uint32_t v[32];
-      tc05::ld_32x32b_x32(tmem + ((uint32_t)(sub * 32) << 16) + (uint32_t)c0, v);
-      tc05::wait_ld();
-      if (KIND == 0) {
-        const int tr = m & 15;
-        const int j = (mtile * 8 + (m >> 4)) * 8 + (tr & 7);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float mine = __uint_as_float(v[c]);
-          const float other = __shfl_xor_sync(0xffffffffu, mine, 8);
-          const int col = c0 + c;
-          if (tr < 8 && col < nvalid) {
-            const float f = __fmul_rn(ts, colf[col]);
-            const float gate = __fmul_rn(mine, f);
-            const float up = __fmul_rn(other, f);
-            const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
-            const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
-            p.h[(size_t)(pair0 + col) * I + j] = *reinterpret_cast<const uint16_t*>(&hv);
+  } else if (warp == 4) {
+    // ---------------- raw weight producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      bool ok = true;
+      const uint64_t pol = l2_evict_first();
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+        const uint8_t* wbase = p.experts + (size_t)it.e * F4_EXPERT + C::BASE + (size_t)it.mtile * 8 * C::TILE;
+        for (int ks = 0; ks < C::NKS; ++ks, ++g) {
+          const uint32_t s = g % RS;
+          if (!wait(&rempty[s], ((g / RS) & 1) ^ 1)) {
+            ok = false;
+            break;
           }
-        }
-      } else {
-        const int orow = mtile * PG_M + m;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = c0 + c;
-          if (col < nvalid) {
-            const float d = __fmul_rn(__uint_as_float(v[c]), ts);
-            atomicAdd(p.yacc + (size_t)coltok[col] * H + orow, __fmul_rn(colf[col], d));
+          uint8_t* dst = rawring + s * G_RAW;
+          mbar_arrive_expect_tx(&rfull[s], G_RAW);
+          const int q = ks >> 2, c4 = ks & 3;
+          for (int r = 0; r < 8; ++r) {
+            const uint8_t* sl = wbase + (size_t)r * C::TILE + (size_t)q * F4_SLICE;
+            bulk_g2s(dst + r * G_RAW_TILE, sl + c4 * 512, 512, &rfull[s], pol);
+            bulk_g2s(dst + r * G_RAW_TILE + 512, sl + F4_CODES, 256, &rfull[s], pol);
           }
         }
       }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        for (uint32_t q = g > RS ? g - RS : 0; q < g; ++q) (void)mbar_wait(&rfull[q % RS], (q / RS) & 1);
+      }
     }
-    tc05::fence_before_sync();
-    failed = __syncthreads_or(failed ? 1 : 0) != 0;
-    tc05::fence_after_sync();
-    if (failed) break;
+  } else if (warp == 5) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      uint32_t g = 0, i_local = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
+        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+        const uint32_t b = i_local & 1, u = i_local >> 1;
+        if (!wait(&accempty[b], (u & 1) ^ 1)) break;
+        tc05::fence_after_sync();
+        const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
+        const uint32_t d = tmem + b * PG_N;
+        for (int ks = 0; ks < C::NKS; ++ks, ++g) {
+          const uint32_t s = g % GS, par = (g / GS) & 1;
+          if (!wait(&afull[s], par) || !wait(&bfull[s], par)) {
+            ok = false;
+            break;
+          }
+          tc05::fence_after_sync();
+          const uint64_t da = tc05::sw128_desc(smem_u32(sm + s * G_STAGE));
+          const uint64_t db = tc05::sw128_desc(smem_u32(sm + s * G_STAGE + G_A));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc05::mma_f16(d, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          tc05::commit(&empty[s]);
+        }
+        if (ok) tc05::commit(&accfull[b]);
+      }
+      if (g > 0) (void)mbar_wait(&empty[(g - 1) % GS], ((g - 1) / GS) & 1);  // last MMAs retired
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ---------------- epilogue (128 threads)
+    const int quad = warp & 3;
+    uint32_t i_local = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++i_local) {
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const uint32_t b = i_local & 1, u = i_local >> 1;
+      const float ts = __ldg(p.tscale + 2 * it.e + KIND);
+      if (!wait(&accfull[b], u & 1)) break;
+      tc05::fence_after_sync();
+      const int m = quad * 32 + lane;  // weight row within the tile
+      for (int c0 = 0; c0 < it.n; c0 += 32) {
+        // per-column token and factor, one column per lane, broadcast below
+        const int pr = it.pair0 + min(c0 + lane, it.nvalid - 1);
+        const int ctok = __ldg(p.pair_token + pr);
+        const float cfac = KIND == 0 ? __fmul_rn(ts, exp2i_p(-__ldg(p.xexp + ctok))) : __ldg(p.pair_w + pr);
+        uint32_t v[32];
+        tc05::ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + b * PG_N + (uint32_t)c0, v);
+        tc05::wait_ld();
+        if (KIND == 0) {
+          // Lane pairs (tr, tr ^ 8) hold the gate and up rows of one
+          // intermediate index j: the low lane finishes even columns, the high
+          // lane odd ones, so every lane works; neighbours (j, j ^ 1) then
+          // store one bf16x2.
+          const int tr = m & 15;
+          const bool lo = tr < 8;
+          const int j = (it.mtile * 8 + (m >> 4)) * 8 + (tr & 7);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const uint32_t send = lo ? v[c + 1] : v[c];
+            const float recv = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 8));
+            const int cc = c + (lo ? 0 : 1);
+            const float f = __shfl_sync(0xffffffffu, cfac, cc);
+            const float gate = __fmul_rn(lo ? __uint_as_float(v[c]) : recv, f);
+            const float up = __fmul_rn(lo ? recv : __uint_as_float(v[c + 1]), f);
+            const float silu = __fdividef(gate, 1.0f + __expf(-gate));
+            const __nv_bfloat16 hv = __float2bfloat16_rn(silu * up);
+            const uint32_t hb = *reinterpret_cast<const uint16_t*>(&hv);
+            const uint32_t nb = __shfl_xor_sync(0xffffffffu, hb, 1);
+            if ((tr & 1) == 0 && c0 + cc < it.nvalid)
+              *reinterpret_cast<uint32_t*>(p.h + (size_t)(it.pair0 + c0 + cc) * I + j) = hb | (nb << 16);
+          }
+        } else {
+          // 4 x 4 transposes among lane quads (two shuffle stages): lane l
+          // ends with rows 4(l/4)..+3 of column 4k + l%4 and adds them with
+          // one 16-byte reduction.
+          const int i1 = lane & 1, p2 = (lane >> 1) & 1;
+          const int orow = it.mtile * PG_M + quad * 32 + (lane & ~3);
+#pragma unroll
+          for (int b4 = 0; b4 < 32; b4 += 4) {
+            const float x0 = __uint_as_float(v[b4]), x1 = __uint_as_float(v[b4 + 1]);
+            const float x2 = __uint_as_float(v[b4 + 2]), x3 = __uint_as_float(v[b4 + 3]);
+            const float ra = __shfl_xor_sync(0xffffffffu, i1 ? x0 : x1, 1);
+            const float rb = __shfl_xor_sync(0xffffffffu, i1 ? x2 : x3, 1);
+            // column (i1): rows (2p, 2p+1) of the quad; column (2 + i1) likewise
+            const float q0a = i1 ? ra : x0, q0b = i1 ? x1 : ra;
+            const float q1a = i1 ? rb : x2, q1b = i1 ? x3 : rb;
+            const float sa = __shfl_xor_sync(0xffffffffu, p2 ? q0a : q1a, 2);
+            const float sb = __shfl_xor_sync(0xffffffffu, p2 ? q0b : q1b, 2);
+            float4 o;
+            o.x = p2 ? sa : q0a;
+            o.y = p2 ? sb : q0b;
+            o.z = p2 ? q1a : sa;
+            o.w = p2 ? q1b : sb;
+            const int cl = b4 + (lane & 3);
+            const int tok = __shfl_sync(0xffffffffu, ctok, cl);
+            const float f = __fmul_rn(__shfl_sync(0xffffffffu, cfac, cl), ts);
+            if (c0 + cl < it.nvalid) {
+              float* dst = p.yacc + (size_t)tok * H + orow;
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__fmul_rn(o.x, f)),
+                           "f"(__fmul_rn(o.y, f)), "f"(__fmul_rn(o.z, f)), "f"(__fmul_rn(o.w, f))
+                           : "memory");
+            }
+          }
+        }
+      }
+      tc05::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[b]);
+    }
+  } else if (warp >= 12) {
+    // ---------------- dequantisers: warp 12 + r owns row tile r of every step
+    const int r = warp - 12;
+    const int g8 = lane >> 2;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int st_row = r * 16 + (mi & 1) * 8 + rr;  // stmatrix row address of this lane
+    uint32_t g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {  // two steps per pass (NKS is even)
+        uint32_t cwv[2][4], scv[2][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t gg = g + h, rs = gg % RS;
+          if (!wait(&rfull[rs], (gg / RS) & 1) || !wait(&empty[gg % GS], ((gg / GS) & 1) ^ 1)) ok = false;
+          if (!ok) break;
+          const int c4 = (ks + h) & 3;
+          const uint8_t* raw = rawring + rs * G_RAW + r * G_RAW_TILE;
+          const uint4 cw = *reinterpret_cast<const uint4*>(raw + lane * 16);
+          const uint2 sc8 = *reinterpret_cast<const uint2*>(raw + 512 + (c4 >> 1) * 128 + g8 * 16 + 8 * (c4 & 1));
+          cwv[h][0] = cw.x;
+          cwv[h][1] = cw.y;
+          cwv[h][2] = cw.z;
+          cwv[h][3] = cw.w;
+          scv[h][0] = sc8.x;
+          scv[h][1] = sc8.y;
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t a_base = smem_u32(sm + ((g + h) % GS) * G_STAGE);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t pair16 = (scv[h][j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
+            const uint32_t sc = e4m3x2_to_f16x2(pair16);
+            float sg = 0.f, sg8 = 0.f;
+            if (KIND == 1) {
+              const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sc));
+              sg = sf.x;
+              sg8 = sf.y;
+            }
+            uint32_t a0, a1, a2, a3;
+            e2m1x8_to_f16x2(cwv[h][j], a0, a1, a2, a3);
+            const uint32_t hi_sc = __byte_perm(sc, 0, 0x3232);
+            // fragments: (row g, k 16j+2t), (row g+8, same k), (row g, k+8), (row g+8, k+8)
+            const uint32_t v0 = dq_pair<KIND>(a0, sc, sg);
+            const uint32_t v1 = dq_pair<KIND>(a1, hi_sc, sg8);
+            const uint32_t v2 = dq_pair<KIND>(a2, sc, sg);
+            const uint32_t v3 = dq_pair<KIND>(a3, hi_sc, sg8);
+            stmatrix_x4(a_base + tc05::sw128_off(st_row, 16 * j + (mi >> 1) * 8), v0, v1, v2, v3);
+          }
+        }
+        tc05::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[g % GS]);
+          mbar_arrive(&afull[(g + 1) % GS]);
+          // the raw slots are released only now: every lane has consumed the
+          // values it loaded from them (an earlier release let the next TMA
+          // copy overwrite a slot under loads still in flight)
+          mbar_arrive(&rempty[g % RS]);
+          mbar_arrive(&rempty[(g + 1) % RS]);
+        }
+      }
+    }
   }
-  if (failed && tid == 0) {
-    // A wait ran out: let the copies and MMAs this CTA issued finish (each
-    // wait again bounded) before the shared and tensor memory are released.
-    for (uint32_t g = raw_issued > PG_RAW ? raw_issued - PG_RAW : 0; g < raw_issued; ++g)
-      (void)mbar_wait(&raw_full[g % PG_RAW], (g / PG_RAW) & 1);
-    if (mma_base > 0) (void)mbar_wait(&mma_bar[(mma_base - 1) % PG_STAGES], ((mma_base - 1) / PG_STAGES) & 1);
-    atomicOr(p.err, ERR_DRAIN);
-  }
+
   tc05::fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 4) {
     tc05::fence_after_sync();
-    tc05::tmem_dealloc(tmem, PG_N);
+    tc05::tmem_dealloc(tmem, 2 * PG_N);
   }
 }
 
@@ -738,9 +863,9 @@ size_t prefill_ws_bytes(int T) {
 }
 
 cudaError_t prefill_kernels_init(int /*device*/) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PG_SMEM);
+  cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PG_SMEM);
+  return cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
 }
 
 cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
@@ -776,11 +901,11 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   gp.err = err;
   gp.prefix = w.gu_prefix;
   gp.bsrc = reinterpret_cast<const uint16_t*>(w.xh16);
-  prefill_gemm_kernel<0><<<sm_count, PG_THREADS, PG_SMEM, st>>>(gp);
+  prefill_gemm_kernel<0><<<sm_count, G_THREADS, G_SMEM, st>>>(gp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gp.prefix = w.dn_prefix;
   gp.bsrc = w.h;
-  prefill_gemm_kernel<1><<<sm_count, PG_THREADS, PG_SMEM, st>>>(gp);
+  prefill_gemm_kernel<1><<<sm_count, G_THREADS, G_SMEM, st>>>(gp);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t n4 = (size_t)T * H / 4;
   prefill_finalize_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(reinterpret_cast<const float4*>(w.yacc),
