@@ -54,6 +54,10 @@ constexpr size_t B16_EXPERT = B16_GU_BYTES + (size_t)DN_TILES * B16_DN_TILE;  //
 constexpr unsigned ERR_WAIT_FULL = 1u;
 constexpr unsigned ERR_WAIT_EMPTY = 2u;
 constexpr unsigned ERR_DRAIN = 4u;
+// The prefill router's tensor-core logit of a candidate expert was further
+// from the exact logit than a quarter of the error bound assumed for it; the
+// token's routing was redone with every logit exact (results stay correct).
+constexpr unsigned ERR_ROUTER_BOUND = 8u;
 
 // A bounded wait gives up after about one second at the maximum SM clock.
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;

@@ -9,10 +9,9 @@
 //   prep            per token: optional RMSNorm (exact), x_hat * 2^e in f16
 //                   with a per-token power-of-two e, and an upper bound on
 //                   ||x_hat||_2
-//   router_approx   fp32 logits S[t][e] by plain fused multiply-adds on CUDA
-//                   cores (sequential over K, so |S - exact| <= gamma_2048 *
-//                   ||x_hat|| * ||W_e|| by the IEEE error bound and
-//                   Cauchy-Schwarz)
+//   gemm<router>    approximate fp32 logits S[t][e] on the tensor cores (bf16
+//                   x_hat and W_r, fp32 accumulation), with an assumed error
+//                   bound 2^-9 * ||x_hat|| * ||W_e|| checked online
 //   route           per token, one warp: the experts whose bound interval can
 //                   reach the 6th largest lower bound are recomputed with an
 //                   error-free sum (TwoSum), every other logit is provably
@@ -39,7 +38,13 @@ namespace {
 constexpr int PG_M = 128;  // weight rows per tile
 constexpr int PG_N = 256;  // tokens per tile
 constexpr int PG_KS = 64;  // K per pipeline step (one 128-byte swizzle row)
-constexpr float GAMMA_K = 1.2300e-4f;           // >= gamma_2048 = 2048 u / (1 - 2048 u), u = 2^-24
+// Error model of the tensor-core router GEMM (bf16 products are exact, fp32
+// accumulation): every one of the 2048 terms is assumed to add at most 2^-20
+// of the sum of |products| to the error, 8 times the worst case of a
+// truncating 24-bit adder.  |S - exact| <= 2048 * 2^-20 * sum|x_k w_k| <=
+// 2^-9 * ||x|| * ||w|| (Cauchy-Schwarz).  The route kernel checks every
+// candidate it recomputes against a quarter of this bound.
+constexpr float GAMMA_TC = 1.953125e-3f;
 
 __device__ __forceinline__ float exp2i_p(int e) { return __int_as_float((127 + e) << 23); }
 
@@ -67,13 +72,20 @@ __device__ __forceinline__ void bf16x8_f32(const uint4 v, float (&f)[8]) {
 __global__ void __launch_bounds__(256) prefill_prep_kernel(const __nv_bfloat16* __restrict__ x,
                                                            const __nv_bfloat16* __restrict__ norm_w, float eps,
                                                            __nv_bfloat16* __restrict__ xh, __half* __restrict__ xh16,
-                                                           int* __restrict__ xexp, float* __restrict__ xnorm) {
+                                                           int* __restrict__ xexp, float* __restrict__ xnorm,
+                                                           int* __restrict__ rprefix, int* __restrict__ roffs,
+                                                           int router_items, int T) {
   __shared__ CSum red[8];
   __shared__ float redf[8];
   __shared__ unsigned redm[8];
   __shared__ float rs;
   const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = tid * 8;
+  if (t == 0)  // the router GEMM's work list: one entry holding every token
+    for (int e = tid; e <= NE; e += 256) {
+      rprefix[e] = e == 0 ? 0 : router_items;
+      roffs[e] = e == 0 ? 0 : T;
+    }
   float v[8];
   bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + k0)), v);
   if (norm_w != nullptr) {
@@ -156,78 +168,6 @@ __global__ void __launch_bounds__(256) prefill_wnorm_kernel(const __nv_bfloat16*
   if (lane == 0) wnorm[e] = sqrtf(s) * 1.001f;
 }
 
-// ---------------------------------------------------------------- router_approx
-// S[t][e] = fp32 sequential fused multiply-add of x_hat[t][k] * W_r[e][k] over
-// k = 0..2047.  CTA tile 128 tokens x 64 experts; thread (ty, tx) owns tokens
-// 8ty..8ty+7 (as 4 packed pairs) and experts 4tx..4tx+3.
-constexpr int RA_TT = 128, RA_TE = 64, RA_KC = 32;
-__global__ void __launch_bounds__(256) prefill_router_approx_kernel(const __nv_bfloat16* __restrict__ xh,
-                                                                    const __nv_bfloat16* __restrict__ wr, int T,
-                                                                    float* __restrict__ S) {
-  __shared__ __align__(16) float xs[RA_KC][RA_TT];      // [k][token]
-  __shared__ __align__(16) float ws[RA_KC][RA_TE * 2];  // [k][expert] duplicated (w, w)
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int t0 = blockIdx.x * RA_TT, e0 = blockIdx.y * RA_TE;
-  uint64_t acc[4][4];  // [token pair][expert]
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0ull;
-  for (int kc = 0; kc < H; kc += RA_KC) {
-    __syncthreads();
-    // x tile: 128 tokens x 32 k = 512 chunks of 8
-    for (int c = tid; c < RA_TT * (RA_KC / 8); c += 256) {
-      const int tt = c >> 2, kk = (c & 3) * 8;
-      const int t = t0 + tt;
-      float f[8];
-      if (t < T) bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(xh + (size_t)t * H + kc + kk)), f);
-      else
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[kk + i][tt] = f[i];
-    }
-    for (int c = tid; c < RA_TE * (RA_KC / 8); c += 256) {
-      const int ee = c >> 2, kk = (c & 3) * 8;
-      float f[8];
-      bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)(e0 + ee) * H + kc + kk)), f);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ws[kk + i][2 * ee] = f[i];
-        ws[kk + i][2 * ee + 1] = f[i];
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < RA_KC; ++k) {
-      const ulonglong2 xa = *reinterpret_cast<const ulonglong2*>(&xs[k][ty * 8]);
-      const ulonglong2 xb = *reinterpret_cast<const ulonglong2*>(&xs[k][ty * 8 + 4]);
-      const ulonglong2 wa = *reinterpret_cast<const ulonglong2*>(&ws[k][tx * 8]);
-      const ulonglong2 wb = *reinterpret_cast<const ulonglong2*>(&ws[k][tx * 8 + 4]);
-      const uint64_t xp[4] = {xa.x, xa.y, xb.x, xb.y};
-      const uint64_t wp[4] = {wa.x, wa.y, wb.x, wb.y};
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint64_t d;
-          asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(xp[a]), "l"(wp[b]), "l"(acc[a][b]));
-          acc[a][b] = d;
-        }
-    }
-  }
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      float lo, hi;
-      f2unpack(acc[a][b], lo, hi);
-      const int t = t0 + ty * 8 + 2 * a, e = e0 + tx * 4 + b;
-      if (t < T) S[(size_t)t * E + e] = lo;
-      if (t + 1 < T) S[(size_t)(t + 1) * E + e] = hi;
-    }
-}
-
 // ---------------------------------------------------------------- route
 // One warp per token.  Lane l holds experts 8l..8l+7.
 __device__ __forceinline__ uint32_t ord_f32(float f) {
@@ -238,7 +178,8 @@ __device__ __forceinline__ uint32_t ord_f32(float f) {
 __global__ void __launch_bounds__(256) prefill_route_kernel(
     const __nv_bfloat16* __restrict__ xh, const __nv_bfloat16* __restrict__ wr, const float* __restrict__ S,
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, int T, int32_t* __restrict__ ids,
-    float* __restrict__ wts, int* __restrict__ counts, int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
+    float* __restrict__ wts, int* __restrict__ counts, int32_t* __restrict__ ids_out, float* __restrict__ w_out,
+    unsigned* __restrict__ err) {
   __shared__ __align__(16) __nv_bfloat16 lrow[8][E];
   __shared__ int sids[8][TOPK];
   __shared__ float sw[8][TOPK];
@@ -258,7 +199,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       sv[i] = s8[i];
-      eps[i] = GAMMA_K * xn * n8[i] * 1.01f;
+      eps[i] = GAMMA_TC * xn * n8[i] * 1.01f;
     }
   }
   // L = 6th largest lower bound (S - eps); ties irrelevant for a bound
@@ -309,24 +250,41 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) xr[j * 8 + i] = f[i];
   }
-  for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
-  __syncwarp();
-  // exact logits of the candidates, one expert at a time across the warp
-  for (int src = 0; src < 32; ++src) {
-    const uint32_t cm = __shfl_sync(0xffffffffu, cand, src);
-    for (uint32_t mm = cm; mm; mm &= mm - 1) {
-      const int e = src * 8 + __ffs(mm) - 1;
-      CSum a = {0.f, 0.f};
+  // Exact logits of the candidates, one expert at a time across the warp;
+  // every other logit is set to -inf.  Returns whether a candidate's
+  // approximate logit missed its exact value by more than a quarter of the
+  // assumed bound (then the error model is in doubt for this token).
+  auto exact_logits = [&](uint32_t cmask) -> bool {
+    for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
+    __syncwarp();
+    bool off = false;
+    for (int src = 0; src < 32; ++src) {
+      const uint32_t cm = __shfl_sync(0xffffffffu, cmask, src);
+      for (uint32_t mm = cm; mm; mm &= mm - 1) {
+        const int e = src * 8 + __ffs(mm) - 1;
+        CSum a = {0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float f[8];
-        bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
+        for (int j = 0; j < 8; ++j) {
+          float f[8];
+          bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
+          for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
+        }
+        a = cs_warp_reduce(a);
+        if (lane == 0) {
+          const float lam = cs_value(a);
+          lrow[warp][e] = __float2bfloat16_rn(lam);
+          const float bound = GAMMA_TC * xn * __ldg(wnorm + e) * 1.01f;
+          if (!(fabsf(__ldg(S + (size_t)t * E + e) - lam) <= 0.25f * bound)) off = true;
+        }
       }
-      a = cs_warp_reduce(a);
-      if (lane == 0) lrow[warp][e] = __float2bfloat16_rn(cs_value(a));
     }
+    __syncwarp();
+    return __any_sync(0xffffffffu, off);
+  };
+  if (exact_logits(cand)) {
+    if (lane == 0) atomicOr(err, ERR_ROUTER_BOUND);
+    if (!all) exact_logits(0xFFu);
   }
   __syncwarp();
   if (lane < 8) umask_dummy[warp][lane] = 0u;
@@ -424,29 +382,33 @@ struct GemmParams {
   const int* xexp;         // [T]
   uint16_t* h;             // gate/up output [P][I]
   float* yacc;             // down output [T][H]
+  const uint16_t* asrc;    // router: W_r bf16 [E][H]
+  float* S;                // router output fp32 [T][E]
   unsigned* err;
 };
 
+// KIND 0: gate/up (NVFP4 -> f16 A, x_hat f16 B), 1: down (NVFP4 -> bf16 A,
+// h bf16 B), 2: router (W_r bf16 A copied as is, x_hat bf16 B, fp32 logits).
 template <int KIND>
 struct GemmCfg {
-  static constexpr int K = KIND == 0 ? H : I;
+  static constexpr int K = KIND == 1 ? I : H;
   static constexpr int NKS = K / PG_KS;
-  static constexpr int MT = (KIND == 0 ? 2 * I : H) / PG_M;
+  static constexpr int MT = (KIND == 0 ? 2 * I : KIND == 1 ? H : E) / PG_M;
   static constexpr int TILE = KIND == 0 ? F4_GU_TILE : F4_DN_TILE;
   static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
 };
 
-constexpr int GS = 4;                          // operand ring stages (one per B producer warp)
-constexpr int RS = 5;                          // raw weight ring slots
+constexpr int AS = 6;                          // A (dequantised weight) ring stages
+constexpr int BS = 3;                          // B (gathered token rows) ring stages, one producer warp each
+constexpr int RPS = 3;                         // raw ring slots, one dequantiser pass (2 K-steps) each
 constexpr int G_THREADS = 640;                 // 20 warps
-constexpr int G_RAW_TILE = 768;                // 512 code bytes + 256 scale bytes of one row tile
+constexpr int G_RAW_TILE = 1152;               // per row tile and pass: 1024 code bytes + 128 scale bytes
 constexpr int G_A = PG_M * PG_KS * 2;          // 16 KB
 constexpr int G_B = PG_N * PG_KS * 2;          // 32 KB
-constexpr int G_STAGE = G_A + G_B;             // 48 KB (1024-byte multiple)
-constexpr int G_RAW = 8 * G_RAW_TILE;          // 6 KB
-static_assert(G_STAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+constexpr int G_RAW = 8 * G_RAW_TILE;          // 9 KB
+static_assert(G_A % 1024 == 0 && G_B % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 static_assert((H / PG_KS) % 2 == 0 && (I / PG_KS) % 2 == 0, "dequantisers take two steps per pass");
-constexpr size_t G_SMEM = 1024 + (size_t)GS * G_STAGE + (size_t)RS * G_RAW + 256;
+constexpr size_t G_SMEM = 1024 + (size_t)AS * G_A + (size_t)BS * G_B + (size_t)RPS * G_RAW + 256;
 static_assert(G_SMEM <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
@@ -493,16 +455,19 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
   using C = GemmCfg<KIND>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* rawring = sm + GS * G_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rawring + RS * G_RAW);
-  uint64_t* bfull = bars;                  // [GS] B rows landed (32 lanes of the stage's producer warp)
-  uint64_t* afull = bars + GS;             // [GS] A stage written (8 dequant warps)
-  uint64_t* empty = bars + 2 * GS;         // [GS] MMAs of the stage done (tcgen05.commit)
-  uint64_t* rfull = bars + 3 * GS;         // [RS] raw bytes landed (TMA transaction count)
-  uint64_t* rempty = bars + 3 * GS + RS;   // [RS] raw slot read (8 dequant warps)
-  uint64_t* accfull = bars + 3 * GS + 2 * RS;       // [2] accumulator complete (tcgen05.commit)
-  uint64_t* accempty = bars + 3 * GS + 2 * RS + 2;  // [2] accumulator read out (4 epilogue warps)
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3 * GS + 2 * RS + 4);
+  uint8_t* aring = sm;                        // [AS][16 KB]
+  uint8_t* bring = sm + AS * G_A;             // [BS][32 KB]
+  uint8_t* rawring = bring + BS * G_B;        // [RPS][9 KB]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rawring + RPS * G_RAW);
+  uint64_t* afull = bars;                     // [AS] A stage written (8 dequant warps)
+  uint64_t* aempty = afull + AS;              // [AS] MMAs reading the A stage done (tcgen05.commit)
+  uint64_t* bfull = aempty + AS;              // [BS] B rows landed (32 lanes of the stage's producer warp)
+  uint64_t* bempty = bfull + BS;              // [BS] MMAs reading the B stage done (tcgen05.commit)
+  uint64_t* rfull = bempty + BS;              // [RPS] raw bytes landed (TMA transaction count)
+  uint64_t* rempty = rfull + RPS;             // [RPS] raw slot consumed (8 dequant warps)
+  uint64_t* accfull = rempty + RPS;           // [2] accumulator complete (tcgen05.commit)
+  uint64_t* accempty = accfull + 2;           // [2] accumulator read out (4 epilogue warps)
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -511,12 +476,15 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     tc05::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < GS; ++i) {
-      mbar_init(&bfull[i], 32);
+    for (int i = 0; i < AS; ++i) {
       mbar_init(&afull[i], 8);
-      mbar_init(&empty[i], 1);
+      mbar_init(&aempty[i], 1);
     }
-    for (int i = 0; i < RS; ++i) {
+    for (int i = 0; i < BS; ++i) {
+      mbar_init(&bfull[i], 32);
+      mbar_init(&bempty[i], 1);
+    }
+    for (int i = 0; i < RPS; ++i) {
       mbar_init(&rfull[i], 1);
       mbar_init(&rempty[i], 8);
     }
@@ -540,8 +508,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     return false;
   };
 
-  if (warp < 4) {
-    // ---------------- B producers: warp w owns operand stage w (steps g = w mod 4)
+  if (warp < BS) {
+    // ---------------- B producers: warp w owns B stage w (steps g = w mod BS)
     uint32_t g = 0;  // global step of this CTA
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -551,16 +519,16 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       for (int i = 0; i < 8; ++i) {
         const int r = lane + 32 * i;
         const int pr = it.pair0 + min(r, it.nvalid - 1);
-        const int row = KIND == 0 ? __ldg(p.pair_token + pr) : pr;
+        const int row = KIND == 0 ? __ldg(p.pair_token + pr) : pr;  // router: the token itself
         src[i] = p.bsrc + (size_t)row * C::K;
       }
       for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-        if ((int)(g % GS) != warp) continue;
-        if (!wait(&empty[warp], ((g / GS) & 1) ^ 1)) {
+        if ((int)(g % BS) != warp) continue;
+        if (!wait(&bempty[warp], ((g / BS) & 1) ^ 1)) {
           ok = false;
           break;
         }
-        uint8_t* dst = sm + warp * G_STAGE + G_A;
+        uint8_t* dst = bring + warp * G_B;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = lane + 32 * i;
@@ -576,33 +544,33 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 4) {
-    // ---------------- raw weight producer
-    if (lane == 0) {
-      uint32_t g = 0;
+    // ---------------- raw weight producer: one slot per dequantiser pass (2 K-steps)
+    if (KIND != 2 && lane == 0) {
+      uint32_t pi = 0;  // global pass
       bool ok = true;
       const uint64_t pol = l2_evict_first();
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
         const uint8_t* wbase = p.experts + (size_t)it.e * F4_EXPERT + C::BASE + (size_t)it.mtile * 8 * C::TILE;
-        for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-          const uint32_t s = g % RS;
-          if (!wait(&rempty[s], ((g / RS) & 1) ^ 1)) {
+        for (int ks = 0; ks < C::NKS; ks += 2, ++pi) {
+          const uint32_t s = pi % RPS;
+          if (!wait(&rempty[s], ((pi / RPS) & 1) ^ 1)) {
             ok = false;
             break;
           }
           uint8_t* dst = rawring + s * G_RAW;
           mbar_arrive_expect_tx(&rfull[s], G_RAW);
-          const int q = ks >> 2, c4 = ks & 3;
+          const int q = ks >> 2, c4 = ks & 3;  // c4 is 0 or 2: both steps share one half of the scales
           for (int r = 0; r < 8; ++r) {
             const uint8_t* sl = wbase + (size_t)r * C::TILE + (size_t)q * F4_SLICE;
-            bulk_g2s(dst + r * G_RAW_TILE, sl + c4 * 512, 512, &rfull[s], pol);
-            bulk_g2s(dst + r * G_RAW_TILE + 512, sl + F4_CODES, 256, &rfull[s], pol);
+            bulk_g2s(dst + r * G_RAW_TILE, sl + c4 * 512, 1024, &rfull[s], pol);
+            bulk_g2s(dst + r * G_RAW_TILE + 1024, sl + F4_CODES + (c4 >> 1) * 128, 128, &rfull[s], pol);
           }
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA exits
-        for (uint32_t q = g > RS ? g - RS : 0; q < g; ++q) (void)mbar_wait(&rfull[q % RS], (q / RS) & 1);
+        for (uint32_t q = pi > RPS ? pi - RPS : 0; q < pi; ++q) (void)mbar_wait(&rfull[q % RPS], (q / RPS) & 1);
       }
     }
   } else if (warp == 5) {
@@ -618,22 +586,23 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
         const uint32_t d = tmem + b * PG_N;
         for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-          const uint32_t s = g % GS, par = (g / GS) & 1;
-          if (!wait(&afull[s], par) || !wait(&bfull[s], par)) {
+          const uint32_t sa = g % AS, sb = g % BS;
+          if (!wait(&afull[sa], (g / AS) & 1) || !wait(&bfull[sb], (g / BS) & 1)) {
             ok = false;
             break;
           }
           tc05::fence_after_sync();
-          const uint64_t da = tc05::sw128_desc(smem_u32(sm + s * G_STAGE));
-          const uint64_t db = tc05::sw128_desc(smem_u32(sm + s * G_STAGE + G_A));
+          const uint64_t da = tc05::sw128_desc(smem_u32(aring + sa * G_A));
+          const uint64_t db = tc05::sw128_desc(smem_u32(bring + sb * G_B));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc05::mma_f16(d, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-          tc05::commit(&empty[s]);
+          tc05::commit(&aempty[sa]);
+          tc05::commit(&bempty[sb]);
         }
         if (ok) tc05::commit(&accfull[b]);
       }
-      if (g > 0) (void)mbar_wait(&empty[(g - 1) % GS], ((g - 1) / GS) & 1);  // last MMAs retired
+      if (g > 0) (void)mbar_wait(&aempty[(g - 1) % AS], ((g - 1) / AS) & 1);  // last MMAs retired
     }
   } else if (warp >= 8 && warp < 12) {
     // ---------------- epilogue (128 threads)
@@ -642,19 +611,27 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++i_local) {
       const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
       const uint32_t b = i_local & 1, u = i_local >> 1;
-      const float ts = __ldg(p.tscale + 2 * it.e + KIND);
+      const float ts = KIND == 2 ? 1.0f : __ldg(p.tscale + 2 * it.e + KIND);
       if (!wait(&accfull[b], u & 1)) break;
       tc05::fence_after_sync();
       const int m = quad * 32 + lane;  // weight row within the tile
       for (int c0 = 0; c0 < it.n; c0 += 32) {
         // per-column token and factor, one column per lane, broadcast below
         const int pr = it.pair0 + min(c0 + lane, it.nvalid - 1);
-        const int ctok = __ldg(p.pair_token + pr);
-        const float cfac = KIND == 0 ? __fmul_rn(ts, exp2i_p(-__ldg(p.xexp + ctok))) : __ldg(p.pair_w + pr);
+        const int ctok = KIND == 2 ? pr : __ldg(p.pair_token + pr);
+        const float cfac = KIND == 0   ? __fmul_rn(ts, exp2i_p(-__ldg(p.xexp + ctok)))
+                           : KIND == 1 ? __ldg(p.pair_w + pr)
+                                       : 1.0f;
         uint32_t v[32];
         tc05::ld_32x32b_x32(tmem + ((uint32_t)(quad * 32) << 16) + b * PG_N + (uint32_t)c0, v);
         tc05::wait_ld();
-        if (KIND == 0) {
+        if (KIND == 2) {
+          // router logits: lanes hold consecutive experts of one token column
+          const int e = it.mtile * PG_M + m;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c0 + c < it.nvalid) p.S[(size_t)(it.pair0 + c0 + c) * E + e] = __uint_as_float(v[c]);
+        } else if (KIND == 0) {
           // Lane pairs (tr, tr ^ 8) hold the gate and up rows of one
           // intermediate index j: the low lane finishes even columns, the high
           // lane odd ones, so every lane works; neighbours (j, j ^ 1) then
@@ -715,7 +692,39 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
     }
-  } else if (warp >= 12) {
+  } else if (KIND == 2 && warp >= 12) {
+    // ---------------- router A producers: warp 12 + r copies rows 16r..16r+15
+    // of the 128-expert tile of W_r, two K-steps per pass
+    const int r = warp - 12;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const uint16_t* arow0 = p.asrc + (size_t)(it.mtile * PG_M + r * 16) * H;
+      for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {
+        if (!wait(&aempty[g % AS], ((g / AS) & 1) ^ 1) || !wait(&aempty[(g + 1) % AS], (((g + 1) / AS) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint8_t* dst = aring + ((g + h) % AS) * G_A;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int idx = lane + 32 * i, row = idx >> 3, ch = idx & 7;
+            cp_async16(dst + tc05::sw128_off(r * 16 + row, ch * 8), arow0 + (size_t)row * H + (ks + h) * PG_KS + ch * 8);
+          }
+        }
+        asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+        tc05::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&afull[g % AS]);
+          mbar_arrive(&afull[(g + 1) % AS]);
+        }
+      }
+    }
+  } else if (KIND != 2 && warp >= 12) {
     // ---------------- dequantisers: warp 12 + r owns row tile r of every step
     const int r = warp - 12;
     const int g8 = lane >> 2;
@@ -725,16 +734,18 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {  // two steps per pass (NKS is even)
+        const uint32_t pi = g >> 1, rs = pi % RPS;
+        if (!wait(&rfull[rs], (pi / RPS) & 1) || !wait(&aempty[g % AS], ((g / AS) & 1) ^ 1) ||
+            !wait(&aempty[(g + 1) % AS], (((g + 1) / AS) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
         uint32_t cwv[2][4], scv[2][2];
+        const uint8_t* raw = rawring + rs * G_RAW + r * G_RAW_TILE;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t gg = g + h, rs = gg % RS;
-          if (!wait(&rfull[rs], (gg / RS) & 1) || !wait(&empty[gg % GS], ((gg / GS) & 1) ^ 1)) ok = false;
-          if (!ok) break;
-          const int c4 = (ks + h) & 3;
-          const uint8_t* raw = rawring + rs * G_RAW + r * G_RAW_TILE;
-          const uint4 cw = *reinterpret_cast<const uint4*>(raw + lane * 16);
-          const uint2 sc8 = *reinterpret_cast<const uint2*>(raw + 512 + (c4 >> 1) * 128 + g8 * 16 + 8 * (c4 & 1));
+          const uint4 cw = *reinterpret_cast<const uint4*>(raw + h * 512 + lane * 16);
+          const uint2 sc8 = *reinterpret_cast<const uint2*>(raw + 1024 + g8 * 16 + 8 * h);
           cwv[h][0] = cw.x;
           cwv[h][1] = cw.y;
           cwv[h][2] = cw.z;
@@ -742,10 +753,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
           scv[h][0] = sc8.x;
           scv[h][1] = sc8.y;
         }
-        if (!ok) break;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const uint32_t a_base = smem_u32(sm + ((g + h) % GS) * G_STAGE);
+          const uint32_t a_base = smem_u32(aring + ((g + h) % AS) * G_A);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t pair16 = (scv[h][j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
@@ -770,13 +780,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         tc05::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&afull[g % GS]);
-          mbar_arrive(&afull[(g + 1) % GS]);
-          // the raw slots are released only now: every lane has consumed the
-          // values it loaded from them (an earlier release let the next TMA
+          mbar_arrive(&afull[g % AS]);
+          mbar_arrive(&afull[(g + 1) % AS]);
+          // the raw slot is released only now: every lane has consumed the
+          // values it loaded from it (an earlier release let the next TMA
           // copy overwrite a slot under loads still in flight)
-          mbar_arrive(&rempty[g % RS]);
-          mbar_arrive(&rempty[(g + 1) % RS]);
+          mbar_arrive(&rempty[(g >> 1) % RPS]);
         }
       }
     }
@@ -823,6 +832,8 @@ struct PrefillWs {
   float* pair_w;      // [7T]
   uint16_t* h;        // [7T][I]
   float* yacc;        // [T][H]
+  int* rprefix;       // [NE + 1] work items of the router GEMM (all under entry 0)
+  int* roffs;         // [NE + 1] its token range: 0 .. T
 };
 
 static PrefillWs carve_prefill(void* ws, int T, size_t* total) {
@@ -852,6 +863,8 @@ static PrefillWs carve_prefill(void* ws, int T, size_t* total) {
   w.pair_w = reinterpret_cast<float*>(take(P * 4));
   w.h = reinterpret_cast<uint16_t*>(take(P * I * 2));
   w.yacc = reinterpret_cast<float*>(take((size_t)T * H * 4));
+  w.rprefix = reinterpret_cast<int*>(take((size_t)(NE + 1) * 4));
+  w.roffs = reinterpret_cast<int*>(take((size_t)(NE + 1) * 4));
   if (total) *total = off;
   return w;
 }
@@ -865,7 +878,9 @@ size_t prefill_ws_bytes(int T) {
 cudaError_t prefill_kernels_init(int /*device*/) {
   cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
+  e = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G_SMEM);
 }
 
 cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
@@ -878,18 +893,26 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   if ((e = cudaMemsetAsync(w.counts, 0, E * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.cursor, 0, E * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.yacc, 0, (size_t)T * H * 4, st)) != cudaSuccess) return e;
-  prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm);
+  const int router_items = ((T + PG_N - 1) / PG_N) * (E / PG_M);
+  prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm, w.rprefix, w.roffs,
+                                         router_items, T);
   prefill_wnorm_kernel<<<E / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(L.router_w), w.wnorm);
-  prefill_router_approx_kernel<<<dim3((T + RA_TT - 1) / RA_TT, E / RA_TE), 256, 0, st>>>(
-      xh, static_cast<const __nv_bfloat16*>(L.router_w), T, w.S);
+  GemmParams gp = {};
+  gp.err = err;
+  gp.prefix = w.rprefix;
+  gp.offsets = w.roffs;
+  gp.bsrc = reinterpret_cast<const uint16_t*>(xh);
+  gp.asrc = static_cast<const uint16_t*>(L.router_w);
+  gp.S = w.S;
+  prefill_gemm_kernel<2><<<sm_count < router_items ? sm_count : router_items, G_THREADS, G_SMEM, st>>>(gp);
   prefill_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(xh, static_cast<const __nv_bfloat16*>(L.router_w), w.S, w.xnorm,
-                                                    w.wnorm, T, w.ids, w.wts, w.counts, ids_out, w_out);
+                                                    w.wnorm, T, w.ids, w.wts, w.counts, ids_out, w_out, err);
   prefill_plan_kernel<<<1, 32 * 9, 0, st>>>(w.counts, T, w.offsets, w.gu_prefix, w.dn_prefix);
   const int nq = T * (TOPK + 1);
   prefill_scatter_kernel<<<(nq + 255) / 256, 256, 0, st>>>(w.ids, w.wts, w.offsets, w.cursor, T, w.pair_token,
                                                             w.pair_w);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  GemmParams gp;
+  gp = GemmParams{};
   gp.experts = L.experts;
   gp.tscale = L.tscale;
   gp.offsets = w.offsets;
