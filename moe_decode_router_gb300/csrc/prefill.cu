@@ -514,14 +514,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
-      const uint16_t* src[8];
+      int rowid[8];  // source row of tile rows lane + 32 i
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int r = lane + 32 * i;
-        const int pr = it.pair0 + min(r, it.nvalid - 1);
-        const int row = KIND == 0 ? __ldg(p.pair_token + pr) : pr;  // router: the token itself
-        src[i] = p.bsrc + (size_t)row * C::K;
+        const int pr = it.pair0 + min(lane + 32 * i, it.nvalid - 1);
+        rowid[i] = KIND == 0 ? __ldg(p.pair_token + pr) : pr;  // router: the token itself
       }
+      const int ch = lane & 7;
       for (int ks = 0; ks < C::NKS; ++ks, ++g) {
         if ((int)(g % BS) != warp) continue;
         if (!wait(&bempty[warp], ((g / BS) & 1) ^ 1)) {
@@ -529,13 +528,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
           break;
         }
         uint8_t* dst = bring + warp * G_B;
+        // 8 lanes per row: one instruction moves 4 whole 128-byte row pieces
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = lane + 32 * i;
-          if (r < it.n) {
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) cp_async16(dst + tc05::sw128_off(r, ch * 8), src[i] + ks * PG_KS + ch * 8);
-          }
+        for (int i = 0; i < PG_N / 4; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          const int row = __shfl_sync(0xffffffffu, rowid[i >> 3], r & 31);
+          if (4 * i < it.n)
+            cp_async16(dst + tc05::sw128_off(r, ch * 8), p.bsrc + (size_t)row * C::K + ks * PG_KS + ch * 8);
         }
         asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
         tc05::fence_proxy_async_smem();
