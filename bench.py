@@ -6,6 +6,7 @@ Workloads (weights drawn on the GPU by the seeded generator, 47 distinct sublaye
   stack47_b1_nvfp4   47 chained NVFP4 sublayers, batch 1     (default)
   stack47_b8_nvfp4   same weights, batch 8
   stack47_b8_bf16    47 chained BF16-expert sublayers, batch 8 (~76 GB)
+  prefill8192_nvfp4  one NVFP4 sublayer over 8,192 tokens (tensor-core grouped GEMMs)
 A step is one pass of the 47-sublayer stack (one CUDA-graph launch of 141
 kernels) over one batch; inputs cycle through 16 seeded batches so routing,
 and hence the experts touched, changes every step.  The resident weights
@@ -45,6 +46,7 @@ WORKLOADS = {
     "stack47_b1_nvfp4": dict(cfg=1, batch=1, fmt="nvfp4"),
     "stack47_b8_nvfp4": dict(cfg=2, batch=8, fmt="nvfp4"),
     "stack47_b8_bf16": dict(cfg=3, batch=8, fmt="bf16"),
+    "prefill8192_nvfp4": dict(cfg=4, batch=8192, fmt="nvfp4", prefill=True),
 }
 METRIC = "MoE decode µs/layer & effective HBM GB/s (% of roofline) at batch 1 and 8"
 
@@ -96,6 +98,48 @@ while True:
 dt = time.perf_counter() - t0
 print(json.dumps({"layers": n, "seconds": dt}))
 """
+
+
+_ORACLE_PREFILL_CHILD = r"""
+import json, sys, time, os
+sys.path.insert(0, os.environ["FLINT_ROOT"])
+import numpy as np, torch
+torch.set_num_threads(1)
+import oracle as O, synth
+cfg, t_small, t_large = int(sys.argv[1]), int(sys.argv[2]), int(sys.argv[3])
+lw = O.layer_from_tensors(synth.gen_layer(cfg, 0, device="cpu"))
+x = synth.gen_x(cfg, t_large, index=0)
+x64 = O.bf16_bits_to_f64(x.view(torch.int16).numpy().view(np.uint16))
+out = {}
+for T in (t_small, t_large):
+    lw.drop_cache()
+    t0 = time.perf_counter()
+    O.moe_prefill(x64[:T], lw)
+    out[str(T)] = time.perf_counter() - t0
+print(json.dumps(out))
+"""
+
+
+def time_oracle_prefill(cfg: int, tokens: int, small: int = 64, large: int = 256) -> dict:
+    """The oracle's expert-grouped prefill on two bounded token counts (single
+    thread); its cost is a per-layer part (every expert dequantised once) plus
+    a per-token part, fitted on the two samples and evaluated at `tokens`."""
+    env = dict(os.environ)
+    env.update(FLINT_ROOT=ROOT, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _ORACLE_PREFILL_CHILD, str(cfg), str(small), str(large)],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    ts, tl = res[str(small)], res[str(large)]
+    per_token = max(0.0, (tl - ts) / (large - small))
+    fixed = max(0.0, ts - per_token * small)
+    us = (fixed + per_token * tokens) * 1e6
+    return dict(value=us, unit="us/layer", cores=1, kind="oracle",
+                sample=f"oracle prefill of {small} and {large} tokens ({ts:.1f} s, {tl:.1f} s single-threaded "
+                       f"numpy fp64); per-layer {fixed:.1f} s + {per_token * 1e3:.2f} ms/token, "
+                       f"evaluated at {tokens} tokens")
 
 
 def time_oracle(cfg: int, batch: int, fmt: str, budget_s: float) -> dict:
@@ -207,7 +251,142 @@ def build_stack(F, synth, torch, wl, dev, n_layers):
     return layers
 
 
+def prefill_flops(T: int) -> float:
+    """Algorithmic FLOPs of one prefill sublayer: router GEMM plus gate/up and
+    down GEMMs over the 6 T routed and T shared token-expert pairs."""
+    H, E, I = 2048, 256, 512
+    return 2.0 * T * E * H + 2.0 * 7 * T * (2 * I * H + H * I)
+
+
+def run_prefill(args, wl):
+    import torch
+    import torch.distributed as tdist
+
+    import synth
+    from moe_decode_router_gb300 import flint_moe as F
+
+    world, rank, local = dist_env()
+    if world > 1:
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    F.load_library()
+    T = wl["batch"]
+    plain = synth.gen_layer(wl["cfg"], 0, device=dev)
+    L = F.pack_layer(plain, device=dev)
+    torch.cuda.synchronize()
+    del plain
+    torch.cuda.empty_cache()
+    n_in = 4
+    xs = [synth.gen_x(wl["cfg"], T, index=i, device=dev) for i in range(n_in)]
+    ys = [torch.empty_like(x) for x in xs]
+    ws = F.alloc_workspace(F.W_NVFP4, T, device=dev)
+    for s in range(max(3, args.warmup)):
+        F.prefill_layer(L, xs[s % n_in], ys[s % n_in], ws)
+    torch.cuda.synchronize()
+    assert F.device_error() == 0
+    steps = args.steps
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(steps):
+        F.prefill_layer(L, xs[s % n_in], ys[s % n_in], ws)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tdist.barrier()
+    clk = clocks.stop()
+    err = F.device_error()
+
+    # End to end through the C ABI: pinned host tokens -> device, sublayer, device -> pinned host.
+    hx = [x.cpu().pin_memory() for x in xs]
+    hy = torch.empty_like(hx[0]).pin_memory()
+    xin = torch.empty_like(xs[0])
+    yout = torch.empty_like(xs[0])
+    for s in range(3):
+        xin.copy_(hx[s % n_in], non_blocking=True)
+        F.prefill_layer(L, xin, yout, ws)
+        hy.copy_(yout, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_steps = max(10, steps // 4)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(e2e_steps):
+        xin.copy_(hx[s % n_in], non_blocking=True)
+        F.prefill_layer(L, xin, yout, ws)
+        hy.copy_(yout, non_blocking=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+
+    ms_t = torch.tensor([ms], device=dev)
+    if world > 1:
+        tdist.all_reduce(ms_t, op=tdist.ReduceOp.MAX)
+    ms_per_step = float(ms_t.item()) / steps
+    flops = prefill_flops(T)
+    tflops = flops / (ms_per_step / 1000.0) / 1e12
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    peak = peaks.get("bf16_tflops_sustained")
+    peak_src = "measured (sustained bf16 cuBLAS)" if peak else "fallback"
+    peak = peak or 1700.0
+    out = {
+        "metric": METRIC,
+        "value": round(ms_per_step * 1000.0, 2),
+        "unit": "us/layer",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4-w/bf16-a (f16/bf16 tensor-core operands, f32 accumulate)",
+        "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
+        "config": {
+            "workload": args.workload, "tokens": T, "hidden": 2048, "experts": "256+1", "inter": 512,
+            "top_k": 6, "weights": "nvfp4", "parallelism": f"replicas x{world}",
+            "l2": "every step streams all 257 experts' packed weights (455 MB) and 4 rotating 32 MB token "
+                  "batches: far larger than L2",
+        },
+        "tflops": round(tflops, 1),
+        "roofline": {
+            "kernel": "prefill sublayer (router GEMM, routing, grouped gate/up and down GEMMs, combine)",
+            "bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(tflops / peak, 4), "peak_source": peak_src,
+            "flops_per_layer": flops, "traffic": None,
+        },
+        "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": "us/layer",
+                "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": T * 2048 * 2},
+        "gpu_launches": steps * 9,
+        "clocks": clk,
+        "device_error_word": err,
+    }
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        try:
+            out["cpu_baseline"] = time_oracle_prefill(wl["cfg"], T)
+        except Exception as e:  # report, do not hide
+            out["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        tdist.destroy_process_group()
+
+
 def run_ours(args):
+    if WORKLOADS[args.workload].get("prefill"):
+        return run_prefill(args, WORKLOADS[args.workload])
     import torch
     import torch.distributed as tdist
 
@@ -366,6 +545,18 @@ def run_reference(args):
     if rank != 0:
         return
     wl = WORKLOADS[args.workload]
+    if wl.get("prefill"):
+        r = time_oracle_prefill(wl["cfg"], wl["batch"])
+        us = r["value"]
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer", "n_gpus": world,
+            "steps": 1, "warmup": 0, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded generator)",
+            "config": {"workload": args.workload, "tokens": wl["batch"], "weights": wl["fmt"]},
+            "cpu_baseline": r,
+            "e2e": {"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(wl["cfg"], wl["batch"], wl["fmt"], per_step_budget / 4)

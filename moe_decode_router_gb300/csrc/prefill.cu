@@ -398,8 +398,8 @@ struct GemmCfg {
   static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
 };
 
-constexpr int AS = 6;                          // A (dequantised weight) ring stages
-constexpr int BS = 3;                          // B (gathered token rows) ring stages, one producer warp each
+constexpr int AS = 4;                          // A (dequantised weight) ring stages
+constexpr int BS = 4;                          // B (gathered token rows) ring stages, one producer warp each
 constexpr int RPS = 3;                         // raw ring slots, one dequantiser pass (2 K-steps) each
 constexpr int G_THREADS = 640;                 // 20 warps
 constexpr int G_RAW_TILE = 1152;               // per row tile and pass: 1024 code bytes + 128 scale bytes
@@ -410,6 +410,19 @@ static_assert(G_A % 1024 == 0 && G_B % 1024 == 0, "stages must keep the 1024-byt
 static_assert((H / PG_KS) % 2 == 0 && (I / PG_KS) % 2 == 0, "dequantisers take two steps per pass");
 constexpr size_t G_SMEM = 1024 + (size_t)AS * G_A + (size_t)BS * G_B + (size_t)RPS * G_RAW + 256;
 static_assert(G_SMEM <= 232448, "shared memory per CTA");
+
+// 16-byte cp.async with an L2 eviction policy (token rows are re-read by
+// every weight-row tile of their expert: keep them in L2).
+__device__ __forceinline__ void cp_async16_keep(void* sdst, const void* gsrc, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(sdst)), "l"(gsrc),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 
 __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
   asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
@@ -512,6 +525,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     // ---------------- B producers: warp w owns B stage w (steps g = w mod BS)
     uint32_t g = 0;  // global step of this CTA
     bool ok = true;
+    const uint64_t keep = l2_evict_last();
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
       int rowid[8];  // source row of tile rows lane + 32 i
@@ -534,7 +548,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
           const int r = 4 * i + (lane >> 3);
           const int row = __shfl_sync(0xffffffffu, rowid[i >> 3], r & 31);
           if (4 * i < it.n)
-            cp_async16(dst + tc05::sw128_off(r, ch * 8), p.bsrc + (size_t)row * C::K + ks * PG_KS + ch * 8);
+            cp_async16_keep(dst + tc05::sw128_off(r, ch * 8), p.bsrc + (size_t)row * C::K + ks * PG_KS + ch * 8, keep);
         }
         asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
         tc05::fence_proxy_async_smem();
