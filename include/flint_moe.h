@@ -145,11 +145,23 @@ int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *la
                            flint_moe_stream_t stream);
 
 /*
- * One MoE sublayer over T tokens (prefill shape, e.g. T = 8192): router GEMM
- * with top-6, tokens grouped by expert, grouped gate/up GEMM with SiLU*up and
- * grouped down GEMM on the tensor cores, weighted combine plus shared expert.
- *   x bf16 [T][H], y bf16 [T][H], topk_ids int32 [T][6] / topk_w fp32 [T][6]
- *   or NULL.  NVFP4 weights only.
+ * One MoE sublayer over T tokens (prefill shape, e.g. T = 8192; "Day-0
+ * Support for Flint on vLLM", section "Optimizations": the MoE kernels also
+ * serve the 8K prefill).  Same definition as flint_moe_decode_layer, token by
+ * token: router logits (approximated on the tensor cores, then recomputed
+ * exactly for every expert that can reach the top 6), sigmoid top-6, tokens
+ * grouped by expert, grouped gate/up GEMM with SiLU*up and grouped down GEMM
+ * on the tensor cores (tcgen05, fp32 accumulation), weighted combine plus the
+ * shared expert.
+ *   x        bf16 [T][H] (RMSNorm'd first if layer->norm_w != NULL)
+ *   y        bf16 [T][H]; must not alias x
+ *   topk_ids int32 [T][6] or NULL; topk_w fp32 [T][6] or NULL
+ *   ws       flint_moe_workspace_bytes(dims, T) bytes, 256-byte aligned, no
+ *            initialisation needed
+ * NVFP4 weights only (BF16: FLINT_MOE_ERR_UNSUPPORTED); 1 <= T <= 2^20.
+ * The combine adds the experts' fp32 contributions in completion order, so y
+ * can differ between runs in its last bits; the routing is exact and
+ * repeatable.  Nine kernels on `stream`, asynchronous.
  */
 int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
                             const void *x, int T, void *y, int32_t *topk_ids,
@@ -190,9 +202,13 @@ int flint_moe_decode_layer_noalloc(const flint_moe_dims *dims, const flint_moe_l
  * before freeing buffers whose addresses a cached stack graph holds. */
 int flint_moe_release(void);
 
-/* Reads (and with reset != 0 clears) the current device's error word, in
- * which a kernel records a bounded wait that gave up.  Synchronises the
- * device.  Returns the word (0 = none) or a negative status. */
+/* Reads (and with reset != 0 clears) the current device's error word.  Bits:
+ * 1, 2, 4 = a bounded wait gave up (full / empty barrier / draining copies);
+ * 8 = the prefill router's tensor-core logit of some expert was further from
+ * the exact value than its assumed error bound allows, and that token's
+ * routing was recomputed from all 256 exact logits (results stay correct).
+ * Synchronises the device.  Returns the word (0 = none) or a negative
+ * status. */
 int flint_moe_device_error(int reset);
 
 /* Static text for a status code. */
