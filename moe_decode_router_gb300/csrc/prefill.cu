@@ -184,11 +184,20 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   __shared__ int sids[8][TOPK];
   __shared__ float sw[8][TOPK];
   __shared__ uint32_t umask_dummy[8][8];
+  __shared__ uint8_t clist[8][E];
+  __shared__ float2 cval[8][E];  // per candidate: (tensor-core logit, its assumed bound)
+  __shared__ float cwn[8][E];    // per candidate: ||W_e|| bound
+  __shared__ uint8_t hlist[8][E];
+  __shared__ int hcount[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const float xn = xnorm[t];
-  float sv[8], eps[8];
+  // the x_hat row is needed later; its loads go out now, with the logits'
+  uint4 xraw[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) xraw[j] = __ldg(reinterpret_cast<const uint4*>(xh + (size_t)t * H) + lane * 8 + j);
+  float sv[8], eps[8], wn8[8];
   {
     const float4 a = __ldg(reinterpret_cast<const float4*>(S + (size_t)t * E + lane * 8));
     const float4 b = __ldg(reinterpret_cast<const float4*>(S + (size_t)t * E + lane * 8 + 4));
@@ -199,6 +208,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       sv[i] = s8[i];
+      wn8[i] = n8[i];
       eps[i] = GAMMA_TC * xn * n8[i] * 1.01f;
     }
   }
@@ -246,38 +256,106 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     float f[8];
-    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(xh + (size_t)t * H) + lane * 8 + j), f);
+    bf16x8_f32(xraw[j], f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) xr[j * 8 + i] = f[i];
   }
-  // Exact logits of the candidates, one expert at a time across the warp;
-  // every other logit is set to -inf.  Returns whether a candidate's
-  // approximate logit missed its exact value by more than a quarter of the
-  // assumed bound (then the error model is in doubt for this token).
+  // Exact bf16 logits of the candidates; every other logit is set to -inf.
+  // Each candidate's dot product is first taken in fp32 with fused
+  // multiply-adds (per lane 4 chains of 16, summed in a 2-level tree, then a
+  // 5-level warp tree: depth 23): its error is at most
+  // gamma_23 * sum|x_k w_k| <= G23 * ||x|| * ||w||.  If both
+  // ends of that interval round to the same bf16 value, so does the exact
+  // logit (rounding is monotone, and the ends are fp32 values obtained with
+  // directed rounding).  Only the rare candidate whose interval straddles a
+  // bf16 rounding boundary is recomputed error-free (TwoSum).  Returns whether
+  // a candidate's tensor-core logit missed it by more than a quarter of the
+  // assumed bound.
+  constexpr float G23 = 1.372e-6f;  // >= gamma_23 = 23 u / (1 - 23 u), u = 2^-24
   auto exact_logits = [&](uint32_t cmask) -> bool {
     for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
+    const int cnt = __popc(cmask);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int n = __shfl_sync(0xffffffffu, incl, 31);
+    int pos = incl - cnt;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((cmask >> i) & 1u) {
+        clist[warp][pos] = (uint8_t)(lane * 8 + i);
+        cval[warp][pos] = make_float2(sv[i], eps[i]);
+        cwn[warp][pos] = wn8[i];
+        ++pos;
+      }
+    if (lane == 0) hcount[warp] = 0;
     __syncwarp();
     bool off = false;
-    for (int src = 0; src < 32; ++src) {
-      const uint32_t cm = __shfl_sync(0xffffffffu, cmask, src);
-      for (uint32_t mm = cm; mm; mm &= mm - 1) {
-        const int e = src * 8 + __ffs(mm) - 1;
-        CSum a = {0.f, 0.f};
+    auto settle = [&](int c, float lam) {  // lane 0: record candidate c's exact logit, check the bound
+      lrow[warp][clist[warp][c]] = __float2bfloat16_rn(lam);
+      const float2 sb = cval[warp][c];
+      if (!(fabsf(sb.x - lam) <= 0.25f * sb.y)) off = true;
+    };
+    for (int ci = 0; ci < n; ci += 2) {
+      const int e0 = clist[warp][ci];
+      const int e1 = ci + 1 < n ? clist[warp][ci + 1] : e0;
+      uint4 w0[8], w1[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float f[8];
-          bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
+      for (int j = 0; j < 8; ++j) {
+        w0[j] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e0 * H) + lane * 8 + j);
+        w1[j] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e1 * H) + lane * 8 + j);
+      }
+      float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};  // chain q: words q of each chunk
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
-        }
-        a = cs_warp_reduce(a);
-        if (lane == 0) {
-          const float lam = cs_value(a);
-          lrow[warp][e] = __float2bfloat16_rn(lam);
-          const float bound = GAMMA_TC * xn * __ldg(wnorm + e) * 1.01f;
-          if (!(fabsf(__ldg(S + (size_t)t * E + e) - lam) <= 0.25f * bound)) off = true;
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a4[4] = {w0[j].x, w0[j].y, w0[j].z, w0[j].w};
+        const uint32_t b4[4] = {w1[j].x, w1[j].y, w1[j].z, w1[j].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float xl = xr[j * 8 + 2 * q], xh2 = xr[j * 8 + 2 * q + 1];
+          p0[q] = fmaf(xl, __uint_as_float(a4[q] << 16), p0[q]);
+          p0[q] = fmaf(xh2, __uint_as_float(a4[q] & 0xFFFF0000u), p0[q]);
+          p1[q] = fmaf(xl, __uint_as_float(b4[q] << 16), p1[q]);
+          p1[q] = fmaf(xh2, __uint_as_float(b4[q] & 0xFFFF0000u), p1[q]);
         }
       }
+      float s0 = __fadd_rn(__fadd_rn(p0[0], p0[1]), __fadd_rn(p0[2], p0[3]));
+      float s1 = __fadd_rn(__fadd_rn(p1[0], p1[1]), __fadd_rn(p1[2], p1[3]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, o));
+        s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, o));
+      }
+      if (lane == 0) {
+        const float sum[2] = {s0, s1};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && ci + 1 >= n) break;
+          const float err = G23 * xn * cwn[warp][ci + h];
+          const __nv_bfloat16 blo = __float2bfloat16_rn(__fsub_rd(sum[h], err));
+          const __nv_bfloat16 bhi = __float2bfloat16_rn(__fadd_ru(sum[h], err));
+          if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(ci + h, sum[h]);
+          else hlist[warp][hcount[warp]++] = (uint8_t)(ci + h);
+        }
+      }
+    }
+    __syncwarp();
+    const int nh = hcount[warp];
+    for (int hi = 0; hi < nh; ++hi) {  // straddling candidates: error-free sum
+      const int c = hlist[warp][hi], e = clist[warp][c];
+      CSum a = {0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float f[8];
+        bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
+      }
+      a = cs_warp_reduce(a);
+      if (lane == 0) settle(c, cs_value(a));  // the rounding of the exact sum
     }
     __syncwarp();
     return __any_sync(0xffffffffu, off);
