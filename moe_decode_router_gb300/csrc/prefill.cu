@@ -441,9 +441,11 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 //               the warp owns the tensor-memory allocation
 //   warp 5      lane 0 issues tcgen05.mma (4 per step) into one of two
 //               256-column fp32 accumulators in tensor memory
-//   warps 8-11  epilogue: tensor memory -> registers (lane quadrant = warp
-//               % 4), SiLU*up -> h (gate/up) or weighted add into the fp32
-//               output (down); overlaps the next item's main loop
+//   warps 8-11, 20-23  epilogue, two sets of 4 warps taking alternate
+//               32-column chunks: tensor memory -> registers (lane quadrant =
+//               warp % 4), SiLU*up -> h (gate/up), weighted add into the fp32
+//               output (down) or the router logits; overlaps the next item's
+//               main loop
 //   warps 12-19 dequantisers: warp 12+r turns row tile r of a step into f16
 //               (gate/up) or bf16 (down) with stmatrix into the
 //               128-byte-swizzled A stage
@@ -479,7 +481,7 @@ struct GemmCfg {
 constexpr int AS = 4;                          // A (dequantised weight) ring stages
 constexpr int BS = 4;                          // B (gathered token rows) ring stages, one producer warp each
 constexpr int RPS = 3;                         // raw ring slots, one dequantiser pass (2 K-steps) each
-constexpr int G_THREADS = 640;                 // 20 warps
+constexpr int G_THREADS = 768;                 // 24 warps
 constexpr int G_RAW_TILE = 1152;               // per row tile and pass: 1024 code bytes + 128 scale bytes
 constexpr int G_A = PG_M * PG_KS * 2;          // 16 KB
 constexpr int G_B = PG_N * PG_KS * 2;          // 32 KB
@@ -557,7 +559,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
   uint64_t* rfull = bempty + BS;              // [RPS] raw bytes landed (TMA transaction count)
   uint64_t* rempty = rfull + RPS;             // [RPS] raw slot consumed (8 dequant warps)
   uint64_t* accfull = rempty + RPS;           // [2] accumulator complete (tcgen05.commit)
-  uint64_t* accempty = accfull + 2;           // [2] accumulator read out (4 epilogue warps)
+  uint64_t* accempty = accfull + 2;           // [2] accumulator read out (8 epilogue warps)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
@@ -581,7 +583,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], 4);
+      mbar_init(&accempty[i], 8);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -695,9 +697,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
       if (g > 0) (void)mbar_wait(&aempty[(g - 1) % AS], ((g - 1) / AS) & 1);  // last MMAs retired
     }
-  } else if (warp >= 8 && warp < 12) {
-    // ---------------- epilogue (128 threads)
-    const int quad = warp & 3;
+  } else if ((warp >= 8 && warp < 12) || warp >= 20) {
+    // ---------------- epilogue: two sets of 4 warps (8-11 and 20-23), each
+    // covering the 4 TMEM lane quadrants; set s takes the 32-column chunks
+    // s, s + 2, s + 4, ... of every item
+    const int quad = warp & 3, eset = warp >= 20 ? 1 : 0;
     uint32_t i_local = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++i_local) {
       const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
@@ -706,7 +710,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       if (!wait(&accfull[b], u & 1)) break;
       tc05::fence_after_sync();
       const int m = quad * 32 + lane;  // weight row within the tile
-      for (int c0 = 0; c0 < it.n; c0 += 32) {
+      for (int c0 = 32 * eset; c0 < it.n; c0 += 64) {
         // per-column token and factor, one column per lane, broadcast below
         const int pr = it.pair0 + min(c0 + lane, it.nvalid - 1);
         const int ctok = KIND == 2 ? pr : __ldg(p.pair_token + pr);
@@ -783,7 +787,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[b]);
     }
-  } else if (KIND == 2 && warp >= 12) {
+  } else if (KIND == 2 && warp >= 12 && warp < 20) {
     // ---------------- router A producers: warp 12 + r copies rows 16r..16r+15
     // of the 128-expert tile of W_r, two K-steps per pass
     const int r = warp - 12;
@@ -815,7 +819,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         }
       }
     }
-  } else if (KIND != 2 && warp >= 12) {
+  } else if (KIND != 2 && warp >= 12 && warp < 20) {
     // ---------------- dequantisers: warp 12 + r owns row tile r of every step
     const int r = warp - 12;
     const int g8 = lane >> 2;
