@@ -430,14 +430,17 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 // One persistent CTA per SM walks work items (expert, token tile, 128-row
 // weight tile), interleaved over CTAs.  Item = D[128 x N] = W[128 x K] *
 // Xg[N x K]^T with N = the tile's token count rounded up to 16, K = 2048
-// (gate/up) or 512 (down), in steps of 64 along K.  Two rings in shared
-// memory: a 4-stage operand ring (dequantised A, gathered B) and a 5-slot
-// ring of raw packed weight bytes.  Warp roles:
+// (gate/up) or 512 (down), in steps of 64 along K.  Rings in shared memory:
+// 4 stages of dequantised A (16 KB), 4 stages of gathered B (32 KB), and 3
+// (down: 2) slots of raw packed weight bytes, one 2-step pass of the 8 row
+// tiles each (9 KB).  The router GEMM uses the same kernel with bf16 router
+// weights copied into A as they are.  Warp roles:
 //   warps 0-3   B producers: warp w gathers the N token rows of every step
-//               g = w (mod 4) into operand stage w with cp.async, waits for
-//               its own copies, fences them for the tensor core and signals
+//               g = w (mod 4) into B stage w with cp.async (8 lanes per
+//               128-byte row piece, L2 evict-last), waits for its own
+//               copies, fences them for the tensor core and signals
 //   warp 4      lane 0 issues the TMA copies of the raw weight bytes of a
-//               step (8 row tiles x (512 code bytes + 256 scale bytes));
+//               pass (8 row tiles x (1024 code bytes + 128 scale bytes));
 //               the warp owns the tensor-memory allocation
 //   warp 5      lane 0 issues tcgen05.mma (4 per step) into one of two
 //               256-column fp32 accumulators in tensor memory
