@@ -17,8 +17,8 @@
 //                   error-free sum (TwoSum), every other logit is provably
 //                   below the 6th; the top-6 then follows the decode path's
 //                   sigmoid top-6 on the exact bf16 logits
-//   plan, scatter   tokens bucketed by expert (routed experts, then the shared
-//                   expert over all tokens), tile counts per expert
+//   scatter         tokens bucketed by expert (routed experts, then the shared
+//                   expert over all tokens), offsets and work-item prefixes
 //   gemm<gate/up>   tcgen05.mma kind::f16 (M=128 weight rows, N=256 tokens,
 //                   fp32 accumulator in tensor memory); NVFP4 weights
 //                   dequantised to f16 (exact) into 128-byte-swizzled shared
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
     const __nv_bfloat16* __restrict__ xh, const __nv_bfloat16* __restrict__ wr, const float* __restrict__ S,
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, int T, int32_t* __restrict__ ids,
     float* __restrict__ wts, int* __restrict__ counts, int32_t* __restrict__ ids_out, float* __restrict__ w_out,
-    unsigned* __restrict__ err) {
+    unsigned* __restrict__ err, float* __restrict__ yacc) {
   __shared__ __align__(16) __nv_bfloat16 lrow[8][E];
   __shared__ int sids[8][TOPK];
   __shared__ float sw[8][TOPK];
@@ -192,6 +192,11 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  // The fp32 output accumulator of this token starts at zero (stores that
+  // overlap this latency-bound kernel instead of a separate memset).
+#pragma unroll
+  for (int j = 0; j < H / 128; ++j)
+    reinterpret_cast<float4*>(yacc + (size_t)t * H)[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float xn = xnorm[t];
   // the x_hat row is needed later; its loads go out now, with the logits'
   uint4 xraw[8];
@@ -381,48 +386,68 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   }
 }
 
-// ---------------------------------------------------------------- plan, scatter
+// ---------------------------------------------------------------- scatter
 // offsets[e]: start of expert e's pairs (experts 0..255 routed, 256 shared);
 // prefix[kind][e]: first work item of expert e (items = tiles of 256 pairs x
 // weight-row tiles of 128).  One CTA.
-__global__ void __launch_bounds__(32 * 9) prefill_plan_kernel(const int* __restrict__ counts, int T,
-                                                              int* __restrict__ offsets, int* __restrict__ gu_prefix,
-                                                              int* __restrict__ dn_prefix) {
-  __shared__ int c[NE];
-  for (int e = threadIdx.x; e < NE; e += blockDim.x) c[e] = e < E ? counts[e] : T;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, gu = 0, dn = 0;
-    for (int e = 0; e < NE; ++e) {
-      offsets[e] = off;
-      gu_prefix[e] = gu;
-      dn_prefix[e] = dn;
-      const int nt = (c[e] + PG_N - 1) / PG_N;
-      off += c[e];
-      gu += nt * (2 * I / PG_M);
-      dn += nt * (H / PG_M);
-    }
-    offsets[NE] = off;
-    gu_prefix[NE] = gu;
-    dn_prefix[NE] = dn;
-  }
-}
-
+// Each block scans the 257 counts itself (exclusive prefix in shared memory);
+// block 0 also publishes the offsets and the work-item prefixes of the two
+// grouped GEMMs.
 __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __restrict__ ids,
                                                               const float* __restrict__ wts,
-                                                              const int* __restrict__ offsets, int* __restrict__ cursor,
-                                                              int T, int* __restrict__ pair_token,
-                                                              float* __restrict__ pair_w) {
-  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+                                                              const int* __restrict__ counts,
+                                                              int* __restrict__ cursor, int T,
+                                                              int* __restrict__ pair_token, float* __restrict__ pair_w,
+                                                              int* __restrict__ offsets, int* __restrict__ gu_prefix,
+                                                              int* __restrict__ dn_prefix) {
+  __shared__ int c[NE + 1];
+  __shared__ int warp_sum[9];
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  // inclusive scan of the counts, 2 per thread (expert 2tid, 2tid+1; 256 = shared)
+  const int e0 = 2 * tid, e1 = 2 * tid + 1;
+  const int v0 = e0 < E ? __ldg(counts + e0) : (e0 == E ? T : 0);
+  const int v1 = e1 < E ? __ldg(counts + e1) : (e1 == E ? T : 0);
+  int incl = v0 + v1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) warp_sum[wp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < wp; ++w) base += warp_sum[w];
+  const int excl = base + incl - v0 - v1;  // offset of expert e0
+  if (e0 <= NE) c[e0] = excl;
+  if (e1 <= NE) c[e1] = excl + v0;
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = tid; e <= NE; e += blockDim.x) {
+      offsets[e] = c[e];
+    }
+    if (tid == 0) {  // work-item prefixes: tiles of PG_N pairs x weight-row tiles
+      int gu = 0, dn = 0;
+      for (int e = 0; e < NE; ++e) {
+        gu_prefix[e] = gu;
+        dn_prefix[e] = dn;
+        const int nt = (c[e + 1] - c[e] + PG_N - 1) / PG_N;
+        gu += nt * (2 * I / PG_M);
+        dn += nt * (H / PG_M);
+      }
+      gu_prefix[NE] = gu;
+      dn_prefix[NE] = dn;
+    }
+  }
+  const int q = blockIdx.x * blockDim.x + tid;
   if (q < T * TOPK) {
     const int t = q / TOPK, e = ids[q];
-    const int pos = offsets[e] + atomicAdd(&cursor[e], 1);
+    const int pos = c[e] + atomicAdd(&cursor[e], 1);
     pair_token[pos] = t;
     pair_w[pos] = wts[q];
   } else if (q < T * (TOPK + 1)) {
     const int t = q - T * TOPK;
-    pair_token[offsets[E] + t] = t;
-    pair_w[offsets[E] + t] = 1.0f;
+    pair_token[c[E] + t] = t;
+    pair_w[c[E] + t] = 1.0f;
   }
 }
 
@@ -990,7 +1015,6 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   cudaError_t e;
   if ((e = cudaMemsetAsync(w.counts, 0, E * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.cursor, 0, E * 4, st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(w.yacc, 0, (size_t)T * H * 4, st)) != cudaSuccess) return e;
   const int router_items = ((T + PG_N - 1) / PG_N) * (E / PG_M);
   prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm, w.rprefix, w.roffs,
                                          router_items, T);
@@ -1004,11 +1028,10 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   gp.S = w.S;
   prefill_gemm_kernel<2><<<sm_count < router_items ? sm_count : router_items, G_THREADS, G_SMEM, st>>>(gp);
   prefill_route_kernel<<<(T + 7) / 8, 256, 0, st>>>(xh, static_cast<const __nv_bfloat16*>(L.router_w), w.S, w.xnorm,
-                                                    w.wnorm, T, w.ids, w.wts, w.counts, ids_out, w_out, err);
-  prefill_plan_kernel<<<1, 32 * 9, 0, st>>>(w.counts, T, w.offsets, w.gu_prefix, w.dn_prefix);
+                                                    w.wnorm, T, w.ids, w.wts, w.counts, ids_out, w_out, err, w.yacc);
   const int nq = T * (TOPK + 1);
-  prefill_scatter_kernel<<<(nq + 255) / 256, 256, 0, st>>>(w.ids, w.wts, w.offsets, w.cursor, T, w.pair_token,
-                                                            w.pair_w);
+  prefill_scatter_kernel<<<(nq + 255) / 256, 256, 0, st>>>(w.ids, w.wts, w.counts, w.cursor, T, w.pair_token,
+                                                            w.pair_w, w.offsets, w.gu_prefix, w.dn_prefix);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   gp = GemmParams{};
   gp.experts = L.experts;
