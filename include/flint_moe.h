@@ -206,7 +206,8 @@ int flint_moe_release(void);
  * 1, 2, 4 = a bounded wait gave up (full / empty barrier / draining copies);
  * 8 = the prefill router's tensor-core logit of some expert was further from
  * the exact value than its assumed error bound allows, and that token's
- * routing was recomputed from all 256 exact logits (results stay correct).
+ * routing was recomputed from all 256 exact logits (results stay correct);
+ * 16 = a prefill kernel found its shared memory misaligned and did nothing.
  * Synchronises the device.  Returns the word (0 = none) or a negative
  * status. */
 int flint_moe_device_error(int reset);

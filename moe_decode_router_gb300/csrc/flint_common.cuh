@@ -58,6 +58,9 @@ constexpr unsigned ERR_DRAIN = 4u;
 // from the exact logit than a quarter of the error bound assumed for it; the
 // token's routing was redone with every logit exact (results stay correct).
 constexpr unsigned ERR_ROUTER_BOUND = 8u;
+// A kernel found its dynamic shared memory misaligned for its layout and did
+// no work.
+constexpr unsigned ERR_LAYOUT = 16u;
 
 // A bounded wait gives up after about one second at the maximum SM clock.
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;

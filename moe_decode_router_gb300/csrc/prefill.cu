@@ -456,12 +456,12 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 // weight tile), interleaved over CTAs.  Item = D[128 x N] = W[128 x K] *
 // Xg[N x K]^T with N = the tile's token count rounded up to 16, K = 2048
 // (gate/up) or 512 (down), in steps of 64 along K.  Rings in shared memory:
-// 4 stages of dequantised A (16 KB), 4 stages of gathered B (32 KB), and 3
-// (down: 2) slots of raw packed weight bytes, one 2-step pass of the 8 row
-// tiles each (9 KB).  The router GEMM uses the same kernel with bf16 router
+// 3 stages of dequantised A (16 KB), 5 stages of gathered B (32 KB), and 2
+// slots of raw packed weight bytes, one 2-step pass of the 8 row tiles each
+// (9 KB).  The router GEMM uses the same kernel with bf16 router
 // weights copied into A as they are.  Warp roles:
-//   warps 0-3   B producers: warp w gathers the N token rows of every step
-//               g = w (mod 4) into B stage w with cp.async (8 lanes per
+//   warps 0-3, 6  B producers: producer i gathers the N token rows of every
+//               step g = i (mod 5) into B stage i with cp.async (8 lanes per
 //               128-byte row piece, L2 evict-last), waits for its own
 //               copies, fences them for the tensor core and signals
 //   warp 4      lane 0 issues the TMA copies of the raw weight bytes of a
@@ -506,9 +506,9 @@ struct GemmCfg {
   static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
 };
 
-constexpr int AS = 4;                          // A (dequantised weight) ring stages
-constexpr int BS = 4;                          // B (gathered token rows) ring stages, one producer warp each
-constexpr int RPS = 3;                         // raw ring slots, one dequantiser pass (2 K-steps) each
+constexpr int AS = 3;                          // A (dequantised weight) ring stages
+constexpr int BS = 5;                          // B (gathered token rows) ring stages, one producer warp each
+constexpr int RPS = 2;                         // raw ring slots, one dequantiser pass (2 K-steps) each
 constexpr int G_THREADS = 768;                 // 24 warps
 constexpr int G_RAW_TILE = 1152;               // per row tile and pass: 1024 code bytes + 128 scale bytes
 constexpr int G_A = PG_M * PG_KS * 2;          // 16 KB
@@ -516,7 +516,9 @@ constexpr int G_B = PG_N * PG_KS * 2;          // 32 KB
 constexpr int G_RAW = 8 * G_RAW_TILE;          // 9 KB
 static_assert(G_A % 1024 == 0 && G_B % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 static_assert((H / PG_KS) % 2 == 0 && (I / PG_KS) % 2 == 0, "dequantisers take two steps per pass");
-constexpr size_t G_SMEM = 1024 + (size_t)AS * G_A + (size_t)BS * G_B + (size_t)RPS * G_RAW + 256;
+// No alignment slack: the dynamic shared memory base is 1024-byte aligned
+// (checked at run time).
+constexpr size_t G_SMEM = (size_t)AS * G_A + (size_t)BS * G_B + (size_t)RPS * G_RAW + 256;
 static_assert(G_SMEM <= 232448, "shared memory per CTA");
 
 // 16-byte cp.async with an L2 eviction policy (token rows are re-read by
@@ -574,8 +576,12 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const int* __restrict_
 template <int KIND>
 __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmParams p) {
   using C = GemmCfg<KIND>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the swizzled stages need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(p.err, ERR_LAYOUT);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* aring = sm;                        // [AS][16 KB]
   uint8_t* bring = sm + AS * G_A;             // [BS][32 KB]
   uint8_t* rawring = bring + BS * G_B;        // [RPS][9 KB]
@@ -629,8 +635,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     return false;
   };
 
-  if (warp < BS) {
-    // ---------------- B producers: warp w owns B stage w (steps g = w mod BS)
+  if (warp < 4 || warp == 6) {
+    // ---------------- B producers: warps 0-3 and 6 own B stages 0-4 (steps g = stage mod BS)
+    const int bp = warp < 4 ? warp : 4;
     uint32_t g = 0;  // global step of this CTA
     bool ok = true;
     const uint64_t keep = l2_evict_last();
@@ -644,12 +651,12 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
       const int ch = lane & 7;
       for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-        if ((int)(g % BS) != warp) continue;
-        if (!wait(&bempty[warp], ((g / BS) & 1) ^ 1)) {
+        if ((int)(g % BS) != bp) continue;
+        if (!wait(&bempty[bp], ((g / BS) & 1) ^ 1)) {
           ok = false;
           break;
         }
-        uint8_t* dst = bring + warp * G_B;
+        uint8_t* dst = bring + bp * G_B;
         // 8 lanes per row: one instruction moves 4 whole 128-byte row pieces
 #pragma unroll
         for (int i = 0; i < PG_N / 4; ++i) {
@@ -660,7 +667,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         }
         asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
         tc05::fence_proxy_async_smem();
-        mbar_arrive(&bfull[warp]);
+        mbar_arrive(&bfull[bp]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
