@@ -429,15 +429,4 @@ __device__ __forceinline__ void zero_routing(Routing& r, int tid, int nthreads) 
   if (tid < 8) r.umask[tid] = 0u;
 }
 
-// Full routing of B tokens by a block of >= 8 warps; ends with __syncthreads.
-__device__ __forceinline__ void compute_routing(const __nv_bfloat16* __restrict__ logits, int B, Routing& r) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  zero_routing(r, tid, blockDim.x);
-  __syncthreads();
-  if (warp < B) warp_topk(load_logits(logits + (size_t)warp * E, lane), lane, r.ids[warp], r.w[warp], r.umask);
-  __syncthreads();
-  if (warp == 0) warp_slot_table(r, B, lane);
-  __syncthreads();
-}
-
 }  // namespace flint

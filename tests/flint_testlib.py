@@ -1,6 +1,6 @@
 """Helpers shared by the parity tests: tolerance checks, routing comparison, runners.
 
-Parity contract (north star of the workload): top-6 ids bit-exact wherever the
+Parity contract (the workload statement's tolerances): top-6 ids bit-exact wherever the
 gap between the 6th and 7th sigmoid score exceeds 1e-3; outputs within
 max|err| <= 2e-2 * rms(ref) and mean|err| <= 2e-3 * rms(ref), rms over the
 oracle output.  Where a token's gap is <= 1e-3 several selections are correct:
