@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
     if (lane == 0) hcount[warp] = 0;
     __syncwarp();
     bool off = false;
-    auto settle = [&](int c, float lam) {  // lane 0: record candidate c's exact logit, check the bound
+    auto settle = [&](int c, float lam) {  // one lane: record candidate c's exact logit, check the bound
       lrow[warp][clist[warp][c]] = __float2bfloat16_rn(lam);
       const float2 sb = cval[warp][c];
       if (!(fabsf(sb.x - lam) <= 0.25f * sb.y)) off = true;
@@ -334,17 +334,13 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
         s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, o));
         s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, o));
       }
-      if (lane == 0) {
-        const float sum[2] = {s0, s1};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (h == 1 && ci + 1 >= n) break;
-          const float err = G23 * xn * cwn[warp][ci + h];
-          const __nv_bfloat16 blo = __float2bfloat16_rn(__fsub_rd(sum[h], err));
-          const __nv_bfloat16 bhi = __float2bfloat16_rn(__fadd_ru(sum[h], err));
-          if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(ci + h, sum[h]);
-          else hlist[warp][hcount[warp]++] = (uint8_t)(ci + h);
-        }
+      if (lane < 2 && ci + lane < n) {  // lane h settles candidate ci + h
+        const float sum = lane == 0 ? s0 : s1;
+        const float err = G23 * xn * cwn[warp][ci + lane];
+        const __nv_bfloat16 blo = __float2bfloat16_rn(__fsub_rd(sum, err));
+        const __nv_bfloat16 bhi = __float2bfloat16_rn(__fadd_ru(sum, err));
+        if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(ci + lane, sum);
+        else hlist[warp][atomicAdd(&hcount[warp], 1)] = (uint8_t)(ci + lane);
       }
     }
     __syncwarp();
@@ -500,6 +496,7 @@ struct GemmParams {
 template <int KIND>
 struct GemmCfg {
   static constexpr int K = KIND == 1 ? I : H;
+  static constexpr int NT = KIND == 2 ? 128 : PG_N;  // tokens per item (router: smaller, more items)
   static constexpr int NKS = K / PG_KS;
   static constexpr int MT = (KIND == 0 ? 2 * I : KIND == 1 ? H : E) / PG_M;
   static constexpr int TILE = KIND == 0 ? F4_GU_TILE : F4_DN_TILE;
@@ -555,7 +552,7 @@ struct ItemInfo {
   int e, mtile, pair0, nvalid, n;  // n = MMA width (nvalid rounded up to 16)
 };
 __device__ __forceinline__ ItemInfo decode_item(int item, const int* __restrict__ prefix,
-                                                const int* __restrict__ offs, int MT) {
+                                                const int* __restrict__ offs, int MT, int NT = PG_N) {
   int lo = 0, hi = NE;  // largest e with prefix[e] <= item
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -567,8 +564,8 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const int* __restrict_
   const int local = item - __ldg(prefix + lo);
   it.mtile = local % MT;
   const int ntile = local / MT;
-  it.pair0 = __ldg(offs + lo) + ntile * PG_N;
-  it.nvalid = min(PG_N, __ldg(offs + lo + 1) - it.pair0);
+  it.pair0 = __ldg(offs + lo) + ntile * NT;
+  it.nvalid = min(NT, __ldg(offs + lo + 1) - it.pair0);
   it.n = (it.nvalid + 15) & ~15;
   return it;
 }
@@ -642,7 +639,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     bool ok = true;
     const uint64_t keep = l2_evict_last();
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
       int rowid[8];  // source row of tile rows lane + 32 i
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -678,7 +675,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       bool ok = true;
       const uint64_t pol = l2_evict_first();
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
         const uint8_t* wbase = p.experts + (size_t)it.e * F4_EXPERT + C::BASE + (size_t)it.mtile * 8 * C::TILE;
         for (int ks = 0; ks < C::NKS; ks += 2, ++pi) {
           const uint32_t s = pi % RPS;
@@ -707,7 +704,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       uint32_t g = 0, i_local = 0;
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
-        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
         const uint32_t b = i_local & 1, u = i_local >> 1;
         if (!wait(&accempty[b], (u & 1) ^ 1)) break;
         tc05::fence_after_sync();
@@ -739,7 +736,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     const int quad = warp & 3, eset = warp >= 20 ? 1 : 0;
     uint32_t i_local = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++i_local) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
       const uint32_t b = i_local & 1, u = i_local >> 1;
       const float ts = KIND == 2 ? 1.0f : __ldg(p.tscale + 2 * it.e + KIND);
       if (!wait(&accfull[b], u & 1)) break;
@@ -829,7 +826,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     uint32_t g = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT);
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
       const uint16_t* arow0 = p.asrc + (size_t)(it.mtile * PG_M + r * 16) * H;
       for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {
         if (!wait(&aempty[g % AS], ((g / AS) & 1) ^ 1) || !wait(&aempty[(g + 1) % AS], (((g + 1) / AS) & 1) ^ 1)) {
@@ -1022,7 +1019,7 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   cudaError_t e;
   if ((e = cudaMemsetAsync(w.counts, 0, E * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.cursor, 0, E * 4, st)) != cudaSuccess) return e;
-  const int router_items = ((T + PG_N - 1) / PG_N) * (E / PG_M);
+  const int router_items = ((T + GemmCfg<2>::NT - 1) / GemmCfg<2>::NT) * (E / PG_M);
   prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm, w.rprefix, w.roffs,
                                          router_items, T);
   prefill_wnorm_kernel<<<E / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(L.router_w), w.wnorm);
