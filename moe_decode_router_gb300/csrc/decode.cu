@@ -493,26 +493,11 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   // only the router's logits, which are final once this wait has returned.
   pdl_trigger();
   const int g = lane >> 2;
-  // The routing input first: the top-k waits on it, the B fragments are needed later.
+  // The routing input first, alone: the top-k waits on it.  The B fragments
+  // (every CTA reads all of x_hat) are requested only after the routing, while
+  // the first routed tiles are in flight.
   uint4 lraw = make_uint4(0u, 0u, 0u, 0u);
   if (warp < B) lraw = load_logits(p.logits + (size_t)warp * E, lane);
-  uint32_t bfr[16][2];
-  if (warp < GU_COMPUTE_WARPS) {
-    if (g < B) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.xfrag + (size_t)(warp * 32 + lane) * 32);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = __ldcg(src + q);
-        bfr[2 * q][0] = v.x;
-        bfr[2 * q][1] = v.y;
-        bfr[2 * q + 1][0] = v.z;
-        bfr[2 * q + 1][1] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int kb = 0; kb < 16; ++kb) bfr[kb][0] = bfr[kb][1] = 0u;
-    }
-  }
   if (warp < B) warp_topk(lraw, lane, R.ids[warp], R.w[warp], R.umask);
   __syncthreads();
   int n_slots = 1;
@@ -553,6 +538,23 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
     return;
   }
 
+  uint32_t bfr[16][2];
+  if (warp < GU_COMPUTE_WARPS) {
+    if (g < B) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.xfrag + (size_t)(warp * 32 + lane) * 32);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = __ldcg(src + q);
+        bfr[2 * q][0] = v.x;
+        bfr[2 * q][1] = v.y;
+        bfr[2 * q + 1][0] = v.z;
+        bfr[2 * q + 1][1] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < 16; ++kb) bfr[kb][0] = bfr[kb][1] = 0u;
+    }
+  }
   if (warp < GU_COMPUTE_WARPS) {
     // ---- compute warps: warp w multiplies K slice w of every tile
     for (int n = 0;; ++n) {
