@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   __shared__ float cwn[8][E];    // per candidate: ||W_e|| bound
   __shared__ uint8_t hlist[8][E];
   __shared__ int hcount[8];
+  __shared__ __align__(16) __nv_bfloat16 xs[8][H];  // x_hat row of each warp's token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
@@ -256,27 +257,25 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   // too many candidates, every logit is computed exactly.
   const bool all = total > 32 || !(L > -80.f && L < 8.f) || fabsf(L) < 4.8828125e-4f;
   if (all) cand = 0xFFu;
-  // x_hat row in registers: 64 elements per lane (lane owns columns 64l..64l+63 as 8 chunks of 8)
-  float xr[64];
+  // x_hat row into the warp's shared-memory slot
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float f[8];
-    bf16x8_f32(xraw[j], f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) xr[j * 8 + i] = f[i];
-  }
+  for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(xs[warp])[lane * 8 + j] = xraw[j];
+  __syncwarp();
   // Exact bf16 logits of the candidates; every other logit is set to -inf.
-  // Each candidate's dot product is first taken in fp32 with fused
-  // multiply-adds (per lane 4 chains of 16, summed in a 2-level tree, then a
-  // 5-level warp tree: depth 23): its error is at most
-  // gamma_23 * sum|x_k w_k| <= G23 * ||x|| * ||w||.  If both
-  // ends of that interval round to the same bf16 value, so does the exact
-  // logit (rounding is monotone, and the ends are fp32 values obtained with
-  // directed rounding).  Only the rare candidate whose interval straddles a
-  // bf16 rounding boundary is recomputed error-free (TwoSum).  Returns whether
-  // a candidate's tensor-core logit missed it by more than a quarter of the
-  // assumed bound.
-  constexpr float G23 = 1.372e-6f;  // >= gamma_23 = 23 u / (1 - 23 u), u = 2^-24
+  // Four candidates at a time, one per group of 8 lanes: lane l of a group
+  // takes columns 64 i + 8 l .. +7 for i = 0..31 (coalesced 128-byte pieces of
+  // the weight row; x_hat from shared memory), in 8 fused multiply-add chains
+  // of 32, then a 3-level tree over the chains and a 3-level tree over the
+  // group (depth 38): the error is at most gamma_38 * sum|x_k w_k| <=
+  // G38 * ||x|| * ||w||, plus 38 * 2^-150 should a step underflow (covered by
+  // an absolute 1e-37).  If both ends of that interval round to the same
+  // bf16 value, so does the exact logit (rounding is monotone, and the ends
+  // are fp32 values obtained with directed rounding).  Only the rare
+  // candidate whose interval straddles a bf16 rounding boundary is
+  // recomputed error-free (TwoSum).  Returns whether a candidate's
+  // tensor-core logit missed it by more than a quarter of the assumed bound.
+  constexpr float G38 = 2.27e-6f;  // >= gamma_38 = 38 u / (1 - 38 u), u = 2^-24
+  const int grp = lane >> 3, gl = lane & 7;
   auto exact_logits = [&](uint32_t cmask) -> bool {
     for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
     const int cnt = __popc(cmask);
@@ -304,56 +303,49 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
       const float2 sb = cval[warp][c];
       if (!(fabsf(sb.x - lam) <= 0.25f * sb.y)) off = true;
     };
-    for (int ci = 0; ci < n; ci += 2) {
-      const int e0 = clist[warp][ci];
-      const int e1 = ci + 1 < n ? clist[warp][ci + 1] : e0;
-      uint4 w0[8], w1[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        w0[j] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e0 * H) + lane * 8 + j);
-        w1[j] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)e1 * H) + lane * 8 + j);
-      }
-      float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};  // chain q: words q of each chunk
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t a4[4] = {w0[j].x, w0[j].y, w0[j].z, w0[j].w};
-        const uint32_t b4[4] = {w1[j].x, w1[j].y, w1[j].z, w1[j].w};
+    const uint4* xv = reinterpret_cast<const uint4*>(xs[warp]);
+    for (int ci = 0; ci < n; ci += 4) {
+      const int c = ci + grp;
+      const int e = clist[warp][c < n ? c : ci];
+      const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
+      float pc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+      for (int i = 0; i < H / 64; ++i) {
+        const uint4 wv = __ldg(wrow + i * 8 + gl);
+        const uint4 x8 = xv[i * 8 + gl];
+        const uint32_t wa[4] = {wv.x, wv.y, wv.z, wv.w};
+        const uint32_t xa[4] = {x8.x, x8.y, x8.z, x8.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float xl = xr[j * 8 + 2 * q], xh2 = xr[j * 8 + 2 * q + 1];
-          p0[q] = fmaf(xl, __uint_as_float(a4[q] << 16), p0[q]);
-          p0[q] = fmaf(xh2, __uint_as_float(a4[q] & 0xFFFF0000u), p0[q]);
-          p1[q] = fmaf(xl, __uint_as_float(b4[q] << 16), p1[q]);
-          p1[q] = fmaf(xh2, __uint_as_float(b4[q] & 0xFFFF0000u), p1[q]);
+          pc[2 * q] = fmaf(__uint_as_float(xa[q] << 16), __uint_as_float(wa[q] << 16), pc[2 * q]);
+          pc[2 * q + 1] =
+              fmaf(__uint_as_float(xa[q] & 0xFFFF0000u), __uint_as_float(wa[q] & 0xFFFF0000u), pc[2 * q + 1]);
         }
       }
-      float s0 = __fadd_rn(__fadd_rn(p0[0], p0[1]), __fadd_rn(p0[2], p0[3]));
-      float s1 = __fadd_rn(__fadd_rn(p1[0], p1[1]), __fadd_rn(p1[2], p1[3]));
+      float sum = __fadd_rn(__fadd_rn(__fadd_rn(pc[0], pc[1]), __fadd_rn(pc[2], pc[3])),
+                            __fadd_rn(__fadd_rn(pc[4], pc[5]), __fadd_rn(pc[6], pc[7])));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        s0 = __fadd_rn(s0, __shfl_xor_sync(0xffffffffu, s0, o));
-        s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, o));
-      }
-      if (lane < 2 && ci + lane < n) {  // lane h settles candidate ci + h
-        const float sum = lane == 0 ? s0 : s1;
-        const float err = G23 * xn * cwn[warp][ci + lane];
+      for (int o = 4; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
+      if (gl == 0 && c < n) {
+        const float err = fmaf(G38 * xn, cwn[warp][c], 1.0e-37f);
         const __nv_bfloat16 blo = __float2bfloat16_rn(__fsub_rd(sum, err));
         const __nv_bfloat16 bhi = __float2bfloat16_rn(__fadd_ru(sum, err));
-        if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(ci + lane, sum);
-        else hlist[warp][atomicAdd(&hcount[warp], 1)] = (uint8_t)(ci + lane);
+        if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(c, sum);
+        else hlist[warp][atomicAdd(&hcount[warp], 1)] = (uint8_t)c;
       }
     }
     __syncwarp();
     const int nh = hcount[warp];
-    for (int hi = 0; hi < nh; ++hi) {  // straddling candidates: error-free sum
+    for (int hi = 0; hi < nh; ++hi) {  // straddling candidates: error-free sum over the whole warp
       const int c = hlist[warp][hi], e = clist[warp][c];
       CSum a = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        float f[8];
+        float f[8], xf[8];
         bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane * 8 + j), f);
+        bf16x8_f32(xv[lane * 8 + j], xf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xr[j * 8 + i], f[i]));
+        for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xf[i], f[i]));
       }
       a = cs_warp_reduce(a);
       if (lane == 0) settle(c, cs_value(a));  // the rounding of the exact sum
@@ -625,6 +617,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
   const uint32_t tmem = *tslot;
   const int n_items = __ldg(p.prefix + NE);
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_try_wait(bar, parity)) return true;  // the usual case: one probe
     if (*abort_flag) return false;
     if (mbar_wait(bar, parity)) return true;
     atomicOr(p.err, ERR_WAIT_FULL);
@@ -699,36 +692,50 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
     }
   } else if (warp == 5) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      uint32_t g = 0, i_local = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
-        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
-        const uint32_t b = i_local & 1, u = i_local >> 1;
-        if (!wait(&accempty[b], (u & 1) ^ 1)) break;
+    // ---------------- MMA issuer.  The whole warp runs the loop, so that the
+    // stage indices, waits and descriptors are warp-uniform values; lane 0
+    // issues the MMAs and the commits (a commit tracks the MMAs of the thread
+    // that issues it).
+    uint32_t g = 0, i_local = 0;
+    uint32_t sa = 0, sb = 0, pa = 0, pb = 0;  // ring stage and phase parity of step g
+    bool ok = true;
+    const uint32_t a0 = smem_u32(aring), b0 = smem_u32(bring);
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
+      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
+      const uint32_t b = i_local & 1, u = i_local >> 1;
+      if (!wait(&accempty[b], (u & 1) ^ 1)) break;
+      tc05::fence_after_sync();
+      const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
+      const uint32_t d = tmem + b * PG_N;
+      for (int ks = 0; ks < C::NKS; ++ks, ++g) {
+        if (!wait(&afull[sa], pa) || !wait(&bfull[sb], pb)) {
+          ok = false;
+          break;
+        }
         tc05::fence_after_sync();
-        const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
-        const uint32_t d = tmem + b * PG_N;
-        for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-          const uint32_t sa = g % AS, sb = g % BS;
-          if (!wait(&afull[sa], (g / AS) & 1) || !wait(&bfull[sb], (g / BS) & 1)) {
-            ok = false;
-            break;
-          }
-          tc05::fence_after_sync();
-          const uint64_t da = tc05::sw128_desc(smem_u32(aring + sa * G_A));
-          const uint64_t db = tc05::sw128_desc(smem_u32(bring + sb * G_B));
+        const uint64_t da = tc05::sw128_desc(a0 + sa * G_A);
+        const uint64_t db = tc05::sw128_desc(b0 + sb * G_B);
+        if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             tc05::mma_f16(d, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           tc05::commit(&aempty[sa]);
           tc05::commit(&bempty[sb]);
         }
-        if (ok) tc05::commit(&accfull[b]);
+        __syncwarp();
+        if (++sa == AS) {
+          sa = 0;
+          pa ^= 1u;
+        }
+        if (++sb == BS) {
+          sb = 0;
+          pb ^= 1u;
+        }
       }
-      if (g > 0) (void)mbar_wait(&aempty[(g - 1) % AS], ((g - 1) / AS) & 1);  // last MMAs retired
+      if (ok && lane == 0) tc05::commit(&accfull[b]);
+      __syncwarp();
     }
+    if (g > 0) (void)mbar_wait(&aempty[(g - 1) % AS], ((g - 1) / AS) & 1);  // last MMAs retired
   } else if ((warp >= 8 && warp < 12) || warp >= 20) {
     // ---------------- epilogue: two sets of 4 warps (8-11 and 20-23), each
     // covering the 4 TMEM lane quadrants; set s takes the 32-column chunks
@@ -862,8 +869,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {  // two steps per pass (NKS is even)
         const uint32_t pi = g >> 1, rs = pi % RPS;
-        if (!wait(&rfull[rs], (pi / RPS) & 1) || !wait(&aempty[g % AS], ((g / AS) & 1) ^ 1) ||
-            !wait(&aempty[(g + 1) % AS], (((g + 1) / AS) & 1) ^ 1)) {
+        if (!wait(&rfull[rs], (pi / RPS) & 1)) {
           ok = false;
           break;
         }
@@ -880,8 +886,14 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
           scv[h][0] = sc8.x;
           scv[h][1] = sc8.y;
         }
+        // Each step's A stage is awaited and published on its own, so that the
+        // dequantisation of a step overlaps the MMAs of the two before it.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          if (!wait(&aempty[(g + h) % AS], (((g + h) / AS) & 1) ^ 1)) {
+            ok = false;
+            break;
+          }
           const uint32_t a_base = smem_u32(aring + ((g + h) % AS) * G_A);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -903,17 +915,15 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
             const uint32_t v3 = dq_pair<KIND>(a3, hi_sc, sg8);
             stmatrix_x4(a_base + tc05::sw128_off(st_row, 16 * j + (mi >> 1) * 8), v0, v1, v2, v3);
           }
+          tc05::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[(g + h) % AS]);
         }
-        tc05::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&afull[g % AS]);
-          mbar_arrive(&afull[(g + 1) % AS]);
-          // the raw slot is released only now: every lane has consumed the
-          // values it loaded from it (an earlier release let the next TMA
-          // copy overwrite a slot under loads still in flight)
-          mbar_arrive(&rempty[(g >> 1) % RPS]);
-        }
+        if (!ok) break;
+        // the raw slot is released only now: every lane has consumed the
+        // values it loaded from it (an earlier release let the next TMA copy
+        // overwrite a slot under loads still in flight)
+        if (lane == 0) mbar_arrive(&rempty[rs]);
       }
     }
   }
