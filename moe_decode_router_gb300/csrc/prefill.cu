@@ -444,19 +444,22 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 // weight tile), interleaved over CTAs.  Item = D[128 x N] = W[128 x K] *
 // Xg[N x K]^T with N = the tile's token count rounded up to 16, K = 2048
 // (gate/up) or 512 (down), in steps of 64 along K.  Rings in shared memory:
-// 3 stages of dequantised A (16 KB), 5 stages of gathered B (32 KB), and 2
-// slots of raw packed weight bytes, one 2-step pass of the 8 row tiles each
-// (9 KB).  The router GEMM uses the same kernel with bf16 router
-// weights copied into A as they are.  Warp roles:
-//   warps 0-3, 6  B producers: producer i gathers the N token rows of every
-//               step g = i (mod 5) into B stage i with cp.async (8 lanes per
+// 4 operand stages, each the dequantised A tile (16 KB) and the gathered B
+// tile (32 KB) of one step, with one "full" barrier (both written) and one
+// "empty" barrier (the step's MMAs done) per stage; and 3 slots of raw
+// packed weight bytes, one 2-step pass of the 8 row tiles each (9 KB).  The
+// router GEMM uses the same kernel with bf16 router weights copied into A as
+// they are.  Warp roles:
+//   warps 0-3   B producers: producer i gathers the N token rows of every
+//               step g = i (mod 4) into B stage i with cp.async (8 lanes per
 //               128-byte row piece, L2 evict-last), waits for its own
 //               copies, fences them for the tensor core and signals
 //   warp 4      lane 0 issues the TMA copies of the raw weight bytes of a
 //               pass (8 row tiles x (1024 code bytes + 128 scale bytes));
 //               the warp owns the tensor-memory allocation
-//   warp 5      lane 0 issues tcgen05.mma (4 per step) into one of two
-//               256-column fp32 accumulators in tensor memory
+//   warp 5      issues tcgen05.mma (4 per step, lane 0) into one of two
+//               256-column fp32 accumulators in tensor memory: one wait and
+//               one commit per step
 //   warps 8-11, 20-23  epilogue, two sets of 4 warps taking alternate
 //               32-column chunks: tensor memory -> registers (lane quadrant =
 //               warp % 4), SiLU*up -> h (gate/up), weighted add into the fp32
@@ -495,9 +498,8 @@ struct GemmCfg {
   static constexpr size_t BASE = KIND == 0 ? 0 : F4_GU_BYTES;
 };
 
-constexpr int AS = 3;                          // A (dequantised weight) ring stages
-constexpr int BS = 5;                          // B (gathered token rows) ring stages, one producer warp each
-constexpr int RPS = 2;                         // raw ring slots, one dequantiser pass (2 K-steps) each
+constexpr int NS = 4;                          // operand ring stages (A and B tile of one K-step), one B producer warp each
+constexpr int RPS = 3;                         // raw ring slots, one dequantiser pass (2 K-steps) each
 constexpr int G_THREADS = 768;                 // 24 warps
 constexpr int G_RAW_TILE = 1152;               // per row tile and pass: 1024 code bytes + 128 scale bytes
 constexpr int G_A = PG_M * PG_KS * 2;          // 16 KB
@@ -507,7 +509,8 @@ static_assert(G_A % 1024 == 0 && G_B % 1024 == 0, "stages must keep the 1024-byt
 static_assert((H / PG_KS) % 2 == 0 && (I / PG_KS) % 2 == 0, "dequantisers take two steps per pass");
 // No alignment slack: the dynamic shared memory base is 1024-byte aligned
 // (checked at run time).
-constexpr size_t G_SMEM = (size_t)AS * G_A + (size_t)BS * G_B + (size_t)RPS * G_RAW + 256;
+constexpr size_t G_TABLES = 2 * (NE + 1) * sizeof(int) + 8;  // item prefixes and pair offsets, copied per CTA
+constexpr size_t G_SMEM = (size_t)NS * (G_A + G_B) + (size_t)RPS * G_RAW + 256 + G_TABLES;
 static_assert(G_SMEM <= 232448, "shared memory per CTA");
 
 // 16-byte cp.async with an L2 eviction policy (token rows are re-read by
@@ -543,21 +546,21 @@ __device__ __forceinline__ uint32_t dq_pair(uint32_t f16pair, uint32_t scale16x2
 struct ItemInfo {
   int e, mtile, pair0, nvalid, n;  // n = MMA width (nvalid rounded up to 16)
 };
-__device__ __forceinline__ ItemInfo decode_item(int item, const int* __restrict__ prefix,
-                                                const int* __restrict__ offs, int MT, int NT = PG_N) {
+// prefix and offs are the CTA's shared-memory copies.
+__device__ __forceinline__ ItemInfo decode_item(int item, const int* prefix, const int* offs, int MT, int NT = PG_N) {
   int lo = 0, hi = NE;  // largest e with prefix[e] <= item
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (__ldg(prefix + mid) <= item) lo = mid;
+    if (prefix[mid] <= item) lo = mid;
     else hi = mid;
   }
   ItemInfo it;
   it.e = lo;
-  const int local = item - __ldg(prefix + lo);
+  const int local = item - prefix[lo];
   it.mtile = local % MT;
   const int ntile = local / MT;
-  it.pair0 = __ldg(offs + lo) + ntile * NT;
-  it.nvalid = min(NT, __ldg(offs + lo + 1) - it.pair0);
+  it.pair0 = offs[lo] + ntile * NT;
+  it.nvalid = min(NT, offs[lo + 1] - it.pair0);
   it.n = (it.nvalid + 15) & ~15;
   return it;
 }
@@ -571,20 +574,20 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     return;
   }
   uint8_t* sm = smem_raw;
-  uint8_t* aring = sm;                        // [AS][16 KB]
-  uint8_t* bring = sm + AS * G_A;             // [BS][32 KB]
-  uint8_t* rawring = bring + BS * G_B;        // [RPS][9 KB]
+  uint8_t* aring = sm;                        // [NS][16 KB]
+  uint8_t* bring = sm + NS * G_A;             // [NS][32 KB]
+  uint8_t* rawring = bring + NS * G_B;        // [RPS][9 KB]
   uint64_t* bars = reinterpret_cast<uint64_t*>(rawring + RPS * G_RAW);
-  uint64_t* afull = bars;                     // [AS] A stage written (8 dequant warps)
-  uint64_t* aempty = afull + AS;              // [AS] MMAs reading the A stage done (tcgen05.commit)
-  uint64_t* bfull = aempty + AS;              // [BS] B rows landed (32 lanes of the stage's producer warp)
-  uint64_t* bempty = bfull + BS;              // [BS] MMAs reading the B stage done (tcgen05.commit)
-  uint64_t* rfull = bempty + BS;              // [RPS] raw bytes landed (TMA transaction count)
+  uint64_t* full = bars;                      // [NS] A tile written (8 warps) and B rows landed (32 lanes)
+  uint64_t* empty = full + NS;                // [NS] MMAs reading the stage done (tcgen05.commit)
+  uint64_t* rfull = empty + NS;               // [RPS] raw bytes landed (TMA transaction count)
   uint64_t* rempty = rfull + RPS;             // [RPS] raw slot consumed (8 dequant warps)
   uint64_t* accfull = rempty + RPS;           // [2] accumulator complete (tcgen05.commit)
   uint64_t* accempty = accfull + 2;           // [2] accumulator read out (8 epilogue warps)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(accempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  int* sprefix = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [NE + 1]
+  int* soffs = sprefix + (NE + 1);                                                // [NE + 1]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == 4) {
@@ -592,13 +595,9 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     tc05::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < AS; ++i) {
-      mbar_init(&afull[i], 8);
-      mbar_init(&aempty[i], 1);
-    }
-    for (int i = 0; i < BS; ++i) {
-      mbar_init(&bfull[i], 32);
-      mbar_init(&bempty[i], 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 8 + 32);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < RPS; ++i) {
       mbar_init(&rfull[i], 1);
@@ -611,11 +610,15 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     *abort_flag = 0;
     fence_mbar_init();
   }
+  for (int i = tid; i <= NE; i += G_THREADS) {  // item decoding then searches shared memory
+    sprefix[i] = __ldg(p.prefix + i);
+    soffs[i] = __ldg(p.offsets + i);
+  }
   tc05::fence_before_sync();
   __syncthreads();
   tc05::fence_after_sync();
   const uint32_t tmem = *tslot;
-  const int n_items = __ldg(p.prefix + NE);
+  const int n_items = sprefix[NE];
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (mbar_try_wait(bar, parity)) return true;  // the usual case: one probe
     if (*abort_flag) return false;
@@ -625,14 +628,14 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     return false;
   };
 
-  if (warp < 4 || warp == 6) {
-    // ---------------- B producers: warps 0-3 and 6 own B stages 0-4 (steps g = stage mod BS)
-    const int bp = warp < 4 ? warp : 4;
+  if (warp < NS) {
+    // ---------------- B producers: warp w owns the B tile of stage w (steps g = w mod NS)
+    const int bp = warp;
     uint32_t g = 0;  // global step of this CTA
     bool ok = true;
     const uint64_t keep = l2_evict_last();
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
+      const ItemInfo it = decode_item(item, sprefix, soffs, C::MT, C::NT);
       int rowid[8];  // source row of tile rows lane + 32 i
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -641,8 +644,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
       const int ch = lane & 7;
       for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-        if ((int)(g % BS) != bp) continue;
-        if (!wait(&bempty[bp], ((g / BS) & 1) ^ 1)) {
+        if ((int)(g % NS) != bp) continue;
+        if (!wait(&empty[bp], ((g / NS) & 1) ^ 1)) {
           ok = false;
           break;
         }
@@ -657,7 +660,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         }
         asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
         tc05::fence_proxy_async_smem();
-        mbar_arrive(&bfull[bp]);
+        mbar_arrive(&full[bp]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -668,7 +671,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       bool ok = true;
       const uint64_t pol = l2_evict_first();
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
+        const ItemInfo it = decode_item(item, sprefix, soffs, C::MT, C::NT);
         const uint8_t* wbase = p.experts + (size_t)it.e * F4_EXPERT + C::BASE + (size_t)it.mtile * 8 * C::TILE;
         for (int ks = 0; ks < C::NKS; ks += 2, ++pi) {
           const uint32_t s = pi % RPS;
@@ -692,50 +695,43 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
     }
   } else if (warp == 5) {
-    // ---------------- MMA issuer.  The whole warp runs the loop, so that the
-    // stage indices, waits and descriptors are warp-uniform values; lane 0
-    // issues the MMAs and the commits (a commit tracks the MMAs of the thread
-    // that issues it).
-    uint32_t g = 0, i_local = 0;
-    uint32_t sa = 0, sb = 0, pa = 0, pb = 0;  // ring stage and phase parity of step g
-    bool ok = true;
-    const uint32_t a0 = smem_u32(aring), b0 = smem_u32(bring);
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
-      const uint32_t b = i_local & 1, u = i_local >> 1;
-      if (!wait(&accempty[b], (u & 1) ^ 1)) break;
-      tc05::fence_after_sync();
-      const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
-      const uint32_t d = tmem + b * PG_N;
-      for (int ks = 0; ks < C::NKS; ++ks, ++g) {
-        if (!wait(&afull[sa], pa) || !wait(&bfull[sb], pb)) {
-          ok = false;
-          break;
-        }
+    // ---------------- MMA issuer (lane 0).  Every item has a multiple of NS
+    // K-steps, so it starts at stage 0 and the loop is unrolled over the
+    // stages: each stage's descriptors are fixed offsets from two base
+    // descriptors, and one wait and one commit cover a step.
+    if (lane == 0) {
+      static_assert(C::NKS % NS == 0, "items must start at ring stage 0");
+      uint32_t i_local = 0, ph = 0, steps = 0;
+      bool ok = true;
+      const uint64_t da0 = tc05::sw128_desc(smem_u32(aring)), db0 = tc05::sw128_desc(smem_u32(bring));
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++i_local) {
+        const ItemInfo it = decode_item(item, sprefix, soffs, C::MT, C::NT);
+        const uint32_t b = i_local & 1, u = i_local >> 1;
+        if (!wait(&accempty[b], (u & 1) ^ 1)) break;
         tc05::fence_after_sync();
-        const uint64_t da = tc05::sw128_desc(a0 + sa * G_A);
-        const uint64_t db = tc05::sw128_desc(b0 + sb * G_B);
-        if (lane == 0) {
+        const uint32_t idesc = tc05::idesc_f16(PG_M, it.n, KIND == 0 ? 0 : 1);
+        const uint32_t d = tmem + b * PG_N;
+        for (int ks = 0; ks < C::NKS && ok; ks += NS) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc05::mma_f16(d, da + (uint64_t)(2 * kk), db + (uint64_t)(2 * kk), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-          tc05::commit(&aempty[sa]);
-          tc05::commit(&bempty[sb]);
+          for (int s = 0; s < NS; ++s) {
+            if (!wait(&full[s], ph)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc05::mma_f16(d, da0 + (uint64_t)(s * (G_A >> 4) + 2 * kk), db0 + (uint64_t)(s * (G_B >> 4) + 2 * kk),
+                            idesc, (ks + s > 0 || kk > 0) ? 1u : 0u);
+            tc05::commit(&empty[s]);
+            ++steps;
+          }
+          ph ^= 1u;
         }
-        __syncwarp();
-        if (++sa == AS) {
-          sa = 0;
-          pa ^= 1u;
-        }
-        if (++sb == BS) {
-          sb = 0;
-          pb ^= 1u;
-        }
+        if (ok) tc05::commit(&accfull[b]);
       }
-      if (ok && lane == 0) tc05::commit(&accfull[b]);
-      __syncwarp();
+      if (steps > 0) (void)mbar_wait(&empty[(steps - 1) % NS], ((steps - 1) / NS) & 1);  // last MMAs retired
     }
-    if (g > 0) (void)mbar_wait(&aempty[(g - 1) % AS], ((g - 1) / AS) & 1);  // last MMAs retired
   } else if ((warp >= 8 && warp < 12) || warp >= 20) {
     // ---------------- epilogue: two sets of 4 warps (8-11 and 20-23), each
     // covering the 4 TMEM lane quadrants; set s takes the 32-column chunks
@@ -743,7 +739,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     const int quad = warp & 3, eset = warp >= 20 ? 1 : 0;
     uint32_t i_local = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++i_local) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
+      const ItemInfo it = decode_item(item, sprefix, soffs, C::MT, C::NT);
       const uint32_t b = i_local & 1, u = i_local >> 1;
       const float ts = KIND == 2 ? 1.0f : __ldg(p.tscale + 2 * it.e + KIND);
       if (!wait(&accfull[b], u & 1)) break;
@@ -833,16 +829,16 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
     uint32_t g = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const ItemInfo it = decode_item(item, p.prefix, p.offsets, C::MT, C::NT);
+      const ItemInfo it = decode_item(item, sprefix, soffs, C::MT, C::NT);
       const uint16_t* arow0 = p.asrc + (size_t)(it.mtile * PG_M + r * 16) * H;
       for (int ks = 0; ks < C::NKS; ks += 2, g += 2) {
-        if (!wait(&aempty[g % AS], ((g / AS) & 1) ^ 1) || !wait(&aempty[(g + 1) % AS], (((g + 1) / AS) & 1) ^ 1)) {
+        if (!wait(&empty[g % NS], ((g / NS) & 1) ^ 1) || !wait(&empty[(g + 1) % NS], (((g + 1) / NS) & 1) ^ 1)) {
           ok = false;
           break;
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint8_t* dst = aring + ((g + h) % AS) * G_A;
+          uint8_t* dst = aring + ((g + h) % NS) * G_A;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int idx = lane + 32 * i, row = idx >> 3, ch = idx & 7;
@@ -853,8 +849,8 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         tc05::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&afull[g % AS]);
-          mbar_arrive(&afull[(g + 1) % AS]);
+          mbar_arrive(&full[g % NS]);
+          mbar_arrive(&full[(g + 1) % NS]);
         }
       }
     }
@@ -890,11 +886,11 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
         // dequantisation of a step overlaps the MMAs of the two before it.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (!wait(&aempty[(g + h) % AS], (((g + h) / AS) & 1) ^ 1)) {
+          if (!wait(&empty[(g + h) % NS], (((g + h) / NS) & 1) ^ 1)) {
             ok = false;
             break;
           }
-          const uint32_t a_base = smem_u32(aring + ((g + h) % AS) * G_A);
+          const uint32_t a_base = smem_u32(aring + ((g + h) % NS) * G_A);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint32_t pair16 = (scv[h][j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
@@ -917,7 +913,7 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
           }
           tc05::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[(g + h) % AS]);
+          if (lane == 0) mbar_arrive(&full[(g + h) % NS]);
         }
         if (!ok) break;
         // the raw slot is released only now: every lane has consumed the
