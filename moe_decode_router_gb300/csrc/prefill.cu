@@ -175,7 +175,7 @@ __device__ __forceinline__ uint32_t ord_f32(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(256) prefill_route_kernel(
+__global__ void __launch_bounds__(256, 4) prefill_route_kernel(
     const __nv_bfloat16* __restrict__ xh, const __nv_bfloat16* __restrict__ wr, const float* __restrict__ S,
     const float* __restrict__ xnorm, const float* __restrict__ wnorm, int T, int32_t* __restrict__ ids,
     float* __restrict__ wts, int* __restrict__ counts, int32_t* __restrict__ ids_out, float* __restrict__ w_out,
@@ -185,19 +185,12 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
   __shared__ float sw[8][TOPK];
   __shared__ uint32_t umask_dummy[8][8];
   __shared__ uint8_t clist[8][E];
-  __shared__ float2 cval[8][E];  // per candidate: (tensor-core logit, its assumed bound)
-  __shared__ float cwn[8][E];    // per candidate: ||W_e|| bound
   __shared__ uint8_t hlist[8][E];
   __shared__ int hcount[8];
   __shared__ __align__(16) __nv_bfloat16 xs[8][H];  // x_hat row of each warp's token
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  // The fp32 output accumulator of this token starts at zero (stores that
-  // overlap this latency-bound kernel instead of a separate memset).
-#pragma unroll
-  for (int j = 0; j < H / 128; ++j)
-    reinterpret_cast<float4*>(yacc + (size_t)t * H)[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float xn = xnorm[t];
   // the x_hat row is needed later; its loads go out now, with the logits'
   uint4 xraw[8];
@@ -291,22 +284,22 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
     for (int i = 0; i < 8; ++i)
       if ((cmask >> i) & 1u) {
         clist[warp][pos] = (uint8_t)(lane * 8 + i);
-        cval[warp][pos] = make_float2(sv[i], eps[i]);
-        cwn[warp][pos] = wn8[i];
         ++pos;
       }
     if (lane == 0) hcount[warp] = 0;
     __syncwarp();
     bool off = false;
-    auto settle = [&](int c, float lam) {  // one lane: record candidate c's exact logit, check the bound
-      lrow[warp][clist[warp][c]] = __float2bfloat16_rn(lam);
-      const float2 sb = cval[warp][c];
-      if (!(fabsf(sb.x - lam) <= 0.25f * sb.y)) off = true;
+    // One lane: record candidate e's exact logit lam; check the tensor-core
+    // logit s_e against the assumed bound (recomputed as in the candidate test).
+    auto settle = [&](int e, float lam, float s_e, float wn_e) {
+      lrow[warp][e] = __float2bfloat16_rn(lam);
+      if (!(fabsf(s_e - lam) <= 0.25f * (GAMMA_TC * xn * wn_e * 1.01f))) off = true;
     };
     const uint4* xv = reinterpret_cast<const uint4*>(xs[warp]);
     for (int ci = 0; ci < n; ci += 4) {
       const int c = ci + grp;
       const int e = clist[warp][c < n ? c : ci];
+      const float s_e = __ldg(S + (size_t)t * E + e), wn_e = __ldg(wnorm + e);
       const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)e * H);
       float pc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
@@ -327,10 +320,10 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
 #pragma unroll
       for (int o = 4; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
       if (gl == 0 && c < n) {
-        const float err = fmaf(G38 * xn, cwn[warp][c], 1.0e-37f);
+        const float err = fmaf(G38 * xn, wn_e, 1.0e-37f);
         const __nv_bfloat16 blo = __float2bfloat16_rn(__fsub_rd(sum, err));
         const __nv_bfloat16 bhi = __float2bfloat16_rn(__fadd_ru(sum, err));
-        if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(c, sum);
+        if (__bfloat16_as_ushort(blo) == __bfloat16_as_ushort(bhi)) settle(e, sum, s_e, wn_e);
         else hlist[warp][atomicAdd(&hcount[warp], 1)] = (uint8_t)c;
       }
     }
@@ -338,6 +331,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
     const int nh = hcount[warp];
     for (int hi = 0; hi < nh; ++hi) {  // straddling candidates: error-free sum over the whole warp
       const int c = hlist[warp][hi], e = clist[warp][c];
+      const float s_e = __ldg(S + (size_t)t * E + e), wn_e = __ldg(wnorm + e);
       CSum a = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -348,7 +342,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
         for (int i = 0; i < 8; ++i) cs_add(a, __fmul_rn(xf[i], f[i]));
       }
       a = cs_warp_reduce(a);
-      if (lane == 0) settle(c, cs_value(a));  // the rounding of the exact sum
+      if (lane == 0) settle(e, cs_value(a), s_e, wn_e);  // the rounding of the exact sum
     }
     __syncwarp();
     return __any_sync(0xffffffffu, off);
@@ -372,6 +366,12 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(
     if (w_out) w_out[(size_t)t * TOPK + lane] = w;
     atomicAdd(&counts[e], 1);
   }
+  // The fp32 output accumulator of this token starts at zero (stores that
+  // overlap this latency-bound kernel instead of a separate memset; issued
+  // last so that they do not queue ahead of the loads above).
+#pragma unroll
+  for (int j = 0; j < H / 128; ++j)
+    reinterpret_cast<float4*>(yacc + (size_t)t * H)[lane + 32 * j] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ---------------------------------------------------------------- scatter
