@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
 //   warp 4      lane 0 issues the TMA copies of the raw weight bytes of a
 //               pass (8 row tiles x (1024 code bytes + 128 scale bytes));
 //               the warp owns the tensor-memory allocation
-//   warp 5      issues tcgen05.mma (4 per step, lane 0) into one of two
+//   warp 5      issues tcgen05.mma (4 per step, one elected lane) into one of two
 //               256-column fp32 accumulators in tensor memory: one wait and
 //               one commit per step
 //   warps 8-11, 20-23  epilogue, two sets of 4 warps taking alternate
@@ -695,11 +695,16 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
       }
     }
   } else if (warp == 5) {
-    // ---------------- MMA issuer (lane 0).  Every item has a multiple of NS
-    // K-steps, so it starts at stage 0 and the loop is unrolled over the
-    // stages: each stage's descriptors are fixed offsets from two base
-    // descriptors, and one wait and one commit cover a step.
-    if (lane == 0) {
+    // ---------------- MMA issuer.  The whole warp runs the loop, so that the
+    // stage indices and descriptors are warp-uniform values; each tcgen05.mma
+    // and tcgen05.commit is issued by the lane elect.sync picks among the
+    // lanes still in the loop.  Normally that is the whole warp; a lane whose
+    // wait runs out leaves on its own, and no elect.sync waits for it.
+    // Every item has a multiple of NS K-steps, so it starts at
+    // stage 0 and the loop is unrolled over the stages: each stage's
+    // descriptors are fixed offsets from two base descriptors, and one wait
+    // and one commit cover a step.
+    {
       static_assert(C::NKS % NS == 0, "items must start at ring stage 0");
       uint32_t i_local = 0, ph = 0, steps = 0;
       bool ok = true;
@@ -719,16 +724,17 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
               break;
             }
             tc05::fence_after_sync();
+            const uint32_t members = __activemask();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              tc05::mma_f16(d, da0 + (uint64_t)(s * (G_A >> 4) + 2 * kk), db0 + (uint64_t)(s * (G_B >> 4) + 2 * kk),
-                            idesc, (ks + s > 0 || kk > 0) ? 1u : 0u);
-            tc05::commit(&empty[s]);
+              tc05::mma_f16_elect(members, d, da0 + (uint64_t)(s * (G_A >> 4) + 2 * kk),
+                                  db0 + (uint64_t)(s * (G_B >> 4) + 2 * kk), idesc, (ks + s > 0 || kk > 0) ? 1u : 0u);
+            tc05::commit_elect(members, &empty[s]);
             ++steps;
           }
           ph ^= 1u;
         }
-        if (ok) tc05::commit(&accfull[b]);
+        if (ok) tc05::commit_elect(__activemask(), &accfull[b]);
       }
       if (steps > 0) (void)mbar_wait(&empty[(steps - 1) % NS], ((steps - 1) / NS) & 1);  // last MMAs retired
     }

@@ -76,6 +76,28 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// The same two instructions issued by one lane of the threads in `members`
+// (all of which must execute the call together, e.g. members = __activemask()):
+// every member executes them, elect.sync picks the issuing lane.  With the
+// same members it picks the same lane every time, so a commit issued this way
+// tracks the MMAs issued this way.  The operands are values every member
+// computed.
+__device__ __forceinline__ void mma_f16_elect(uint32_t members, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, %5;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(members)
+      : "memory");
+}
+__device__ __forceinline__ void commit_elect(uint32_t members, uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, %1;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar)),
+      "r"(members)
+      : "memory");
+}
+
 // Arrives (once) on an mbarrier when all previously issued MMAs of this thread completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
