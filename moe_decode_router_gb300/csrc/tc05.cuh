@@ -66,22 +66,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (M x N x 16), issued by one thread.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two instructions issued by one lane of the threads in `members`
-// (all of which must execute the call together, e.g. members = __activemask()):
-// every member executes them, elect.sync picks the issuing lane.  With the
-// same members it picks the same lane every time, so a commit issued this way
-// tracks the MMAs issued this way.  The operands are values every member
-// computed.
+// D[tmem] (+)= A[smem] * B[smem]^T, one instruction (M x N x 16), issued by
+// one lane of the threads in `members` (all of which must execute the call
+// together, e.g. members = __activemask()): every member executes it and
+// elect.sync picks the issuing lane.  With the same members it picks the same
+// lane every time, which matters for commit_elect below.  The operands are
+// values every member computed.
 __device__ __forceinline__ void mma_f16_elect(uint32_t members, uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -90,19 +80,16 @@ __device__ __forceinline__ void mma_f16_elect(uint32_t members, uint32_t d_tmem,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(members)
       : "memory");
 }
+
+// Arrives (once) on an mbarrier when all MMAs previously issued by the issuing
+// thread have completed; the issuing lane is elected as in mma_f16_elect, so
+// with the same members the commit tracks the MMAs issued that way.
 __device__ __forceinline__ void commit_elect(uint32_t members, uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred e;\n elect.sync _|e, %1;\n"
       " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar)),
       "r"(members)
       : "memory");
-}
-
-// Arrives (once) on an mbarrier when all previously issued MMAs of this thread completed.
-__device__ __forceinline__ void commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
 }
 
 // 32 consecutive 32-bit TMEM columns of the warp's 32 lanes (lane i -> thread i).
