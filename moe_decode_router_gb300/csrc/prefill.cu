@@ -413,17 +413,29 @@ __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __r
     for (int e = tid; e <= NE; e += blockDim.x) {
       offsets[e] = c[e];
     }
-    if (tid == 0) {  // work-item prefixes: tiles of PG_N pairs x weight-row tiles
-      int gu = 0, dn = 0;
-      for (int e = 0; e < NE; ++e) {
-        gu_prefix[e] = gu;
-        dn_prefix[e] = dn;
-        const int nt = (c[e + 1] - c[e] + PG_N - 1) / PG_N;
-        gu += nt * (2 * I / PG_M);
-        dn += nt * (H / PG_M);
-      }
-      gu_prefix[NE] = gu;
-      dn_prefix[NE] = dn;
+    // work-item prefixes: exclusive scan of each expert's tiles of PG_N pairs
+    // (entry NE = the total), times the weight-row tiles of each GEMM
+    const int n0 = e0 < NE ? (c[e0 + 1] - c[e0] + PG_N - 1) / PG_N : 0;
+    const int n1 = e1 < NE ? (c[e1 + 1] - c[e1] + PG_N - 1) / PG_N : 0;
+    int tin = n0 + n1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, tin, off);
+      if (lane >= off) tin += u;
+    }
+    __syncthreads();  // every thread has read warp_sum above
+    if (lane == 31) warp_sum[wp] = tin;
+    __syncthreads();
+    int tbase = 0;
+    for (int w = 0; w < wp; ++w) tbase += warp_sum[w];
+    const int t0 = tbase + tin - n0 - n1;  // tiles before expert e0
+    if (e0 <= NE) {
+      gu_prefix[e0] = t0 * (2 * I / PG_M);
+      dn_prefix[e0] = t0 * (H / PG_M);
+    }
+    if (e1 <= NE) {
+      gu_prefix[e1] = (t0 + n0) * (2 * I / PG_M);
+      dn_prefix[e1] = (t0 + n0) * (H / PG_M);
     }
   }
   const int q = blockIdx.x * blockDim.x + tid;
