@@ -369,7 +369,7 @@ def run_prefill(args, wl):
         },
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": "us/layer",
                 "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": T * 2048 * 2},
-        "gpu_launches": steps * 8,
+        "gpu_launches": steps * 7,
         "clocks": clk,
         "device_error_word": err,
     }

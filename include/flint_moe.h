@@ -161,7 +161,7 @@ int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *la
  * NVFP4 weights only (BF16: FLINT_MOE_ERR_UNSUPPORTED); 1 <= T <= 2^20.
  * The combine adds the experts' fp32 contributions in completion order, so y
  * can differ between runs in its last bits; the routing is exact and
- * repeatable.  Eight kernels on `stream`, asynchronous.
+ * repeatable.  Seven kernels on `stream`, asynchronous.
  */
 int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
                             const void *x, int T, void *y, int32_t *topk_ids,

@@ -69,17 +69,41 @@ __device__ __forceinline__ void bf16x8_f32(const uint4 v, float (&f)[8]) {
 
 // ---------------------------------------------------------------- prep
 // One CTA (256 threads, 8 columns each) per token.
+// Upper bound on ||W_r[e]||_2 for experts 8 wb .. 8 wb + 7, one warp each.
+__device__ __forceinline__ void wnorm_rows(const __nv_bfloat16* __restrict__ wr, float* __restrict__ wnorm, int wb) {
+  const int e = wb * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= E) return;
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float f[8];
+    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane + 32 * j), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s = fmaf(f[i], f[i], s);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) wnorm[e] = sqrtf(s) * 1.001f;
+}
+
 __global__ void __launch_bounds__(256) prefill_prep_kernel(const __nv_bfloat16* __restrict__ x,
                                                            const __nv_bfloat16* __restrict__ norm_w, float eps,
                                                            __nv_bfloat16* __restrict__ xh, __half* __restrict__ xh16,
                                                            int* __restrict__ xexp, float* __restrict__ xnorm,
                                                            int* __restrict__ rprefix, int* __restrict__ roffs,
-                                                           int router_items, int T) {
+                                                           int router_items, int T,
+                                                           const __nv_bfloat16* __restrict__ wr, float* __restrict__ wnorm) {
   __shared__ CSum red[8];
   __shared__ float redf[8];
   __shared__ unsigned redm[8];
   __shared__ float rs;
-  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // The first E / 8 blocks bound the router rows' norms; the others handle
+  // one token each.
+  if (blockIdx.x < E / 8) {
+    wnorm_rows(wr, wnorm, blockIdx.x);
+    return;
+  }
+  const int t = blockIdx.x - E / 8, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = tid * 8;
   if (t == 0)  // the router GEMM's work list: one entry holding every token
     for (int e = tid; e <= NE; e += 256) {
@@ -151,22 +175,6 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(const __nv_bfloat16* 
   *reinterpret_cast<uint4*>(xh16 + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
-// Upper bound on ||W_r[e]||_2, one warp per expert.
-__global__ void __launch_bounds__(256) prefill_wnorm_kernel(const __nv_bfloat16* __restrict__ wr, float* __restrict__ wnorm) {
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (e >= E) return;
-  float s = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float f[8];
-    bf16x8_f32(__ldg(reinterpret_cast<const uint4*>(wr + (size_t)e * H) + lane + 32 * j), f);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s = fmaf(f[i], f[i], s);
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) wnorm[e] = sqrtf(s) * 1.001f;
-}
 
 // ---------------------------------------------------------------- route
 // One warp per token.  Lane l holds experts 8l..8l+7.
@@ -1044,9 +1052,9 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
   if ((e = cudaMemsetAsync(w.counts, 0, E * 4, st)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(w.cursor, 0, E * 4, st)) != cudaSuccess) return e;
   const int router_items = ((T + GemmCfg<2>::NT - 1) / GemmCfg<2>::NT) * (E / PG_M);
-  prefill_prep_kernel<<<T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm, w.rprefix, w.roffs,
-                                         router_items, T);
-  prefill_wnorm_kernel<<<E / 8, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(L.router_w), w.wnorm);
+  prefill_prep_kernel<<<E / 8 + T, 256, 0, st>>>(xin, norm, eps, w.xh, w.xh16, w.xexp, w.xnorm, w.rprefix, w.roffs,
+                                                 router_items, T, static_cast<const __nv_bfloat16*>(L.router_w),
+                                                 w.wnorm);
   GemmParams gp = {};
   gp.err = err;
   gp.prefix = w.rprefix;
