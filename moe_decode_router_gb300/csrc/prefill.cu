@@ -8,13 +8,15 @@
 //
 //   prep            per token: optional RMSNorm (exact), x_hat * 2^e in f16
 //                   with a per-token power-of-two e, and an upper bound on
-//                   ||x_hat||_2
+//                   ||x_hat||_2; 32 more blocks bound every ||W_r[e]||_2
 //   gemm<router>    approximate fp32 logits S[t][e] on the tensor cores (bf16
 //                   x_hat and W_r, fp32 accumulation), with an assumed error
 //                   bound 2^-9 * ||x_hat|| * ||W_e|| checked online
 //   route           per token, one warp: the experts whose bound interval can
-//                   reach the 6th largest lower bound are recomputed with an
-//                   error-free sum (TwoSum), every other logit is provably
+//                   reach the 6th largest lower bound get their exact bf16
+//                   logit (an fp32 dot product with a rigorous error interval,
+//                   or an error-free TwoSum sum where that interval straddles
+//                   a bf16 rounding boundary); every other logit is provably
 //                   below the 6th; the top-6 then follows the decode path's
 //                   sigmoid top-6 on the exact bf16 logits
 //   scatter         tokens bucketed by expert (routed experts, then the shared
@@ -385,10 +387,10 @@ __global__ void __launch_bounds__(256, 4) prefill_route_kernel(
 // ---------------------------------------------------------------- scatter
 // offsets[e]: start of expert e's pairs (experts 0..255 routed, 256 shared);
 // prefix[kind][e]: first work item of expert e (items = tiles of 256 pairs x
-// weight-row tiles of 128).  One CTA.
-// Each block scans the 257 counts itself (exclusive prefix in shared memory);
-// block 0 also publishes the offsets and the work-item prefixes of the two
-// grouped GEMMs.
+// weight-row tiles of 128).  One thread per (token, expert) pair.  Each block
+// scans the 257 counts itself (exclusive prefix in shared memory); block 0
+// also publishes the offsets and the work-item prefixes of the two grouped
+// GEMMs.
 __global__ void __launch_bounds__(256) prefill_scatter_kernel(const int32_t* __restrict__ ids,
                                                               const float* __restrict__ wts,
                                                               const int* __restrict__ counts,
