@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(256, 4) prefill_route_kernel(
   // recomputed error-free (TwoSum).  Returns whether a candidate's
   // tensor-core logit missed it by more than a quarter of the assumed bound.
   constexpr float G38 = 2.27e-6f;  // >= gamma_38 = 38 u / (1 - 38 u), u = 2^-24
+  static_assert((double)G38 >= 38.0 / 16777216.0 / (1.0 - 38.0 / 16777216.0), "G38 must bound gamma_38");
   const int grp = lane >> 3, gl = lane & 7;
   auto exact_logits = [&](uint32_t cmask) -> bool {
     for (int i = lane; i < E; i += 32) lrow[warp][i] = __float2bfloat16_rn(-INFINITY);
