@@ -99,3 +99,29 @@ def check_layer(x_in: np.ndarray, lw: "O.LayerView", gpu_y: np.ndarray, gpu_ids:
     stats = check_output(gpu_y, ref["y"])
     stats["near_ties"] = len(forced)
     return ref, stats
+
+
+def prefill_reference_rows(x64: np.ndarray, lw: "O.LayerView", gpu_ids: np.ndarray):
+    """Oracle y and weights for the rows of x64, from the expert-grouped
+    definition.  Where a token's 6th/7th score gap is within the tolerance, the
+    GPU's (valid) selection replaces the oracle's and that token is recomputed
+    with it.  Returns (y, weights, number of such tokens)."""
+    ref = O.moe_prefill(x64, lw)
+    forced = compare_routing(ref, gpu_ids)
+    y, w = ref["y"].copy(), ref["weights"].copy()
+    for t, sel in forced.items():
+        sub = O.moe_layer(x64[t:t + 1], lw, forced={0: sel})
+        y[t], w[t] = sub["y"][0], sub["weights"][0]
+        lw.drop_cache()
+    lw.drop_cache()
+    return y, w, len(forced)
+
+
+def check_prefill(x: torch.Tensor, lw: "O.LayerView", y: torch.Tensor, ids: np.ndarray, w: np.ndarray) -> dict:
+    """Routing, routing weights and outputs of a prefill call against the oracle."""
+    x64 = bf16_to_f64(x)
+    y_ref, w_ref, n_forced = prefill_reference_rows(x64, lw, ids)
+    assert np.allclose(w, w_ref, rtol=1e-6, atol=1e-7)
+    st = check_output(bf16_to_f64(y), y_ref)
+    st["near_ties"] = n_forced
+    return st

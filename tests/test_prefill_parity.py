@@ -15,7 +15,7 @@ import torch
 
 import oracle as O
 import synth
-from flint_testlib import bf16_to_f64, check_output, compare_routing
+from flint_testlib import bf16_to_f64, check_output, check_prefill, compare_routing
 from moe_decode_router_gb300 import flint_moe as F
 
 pytestmark = pytest.mark.gpu
@@ -59,30 +59,6 @@ def run_prefill(L, x, dev, ws=None):
     torch.cuda.synchronize()
     assert F.device_error() == 0
     return y, ids.cpu().numpy(), w.cpu().numpy()
-
-
-def reference_rows(x64, lw, gpu_ids):
-    """Oracle y, ids and weights for the rows of x64.  Where a token's 6th/7th
-    score gap is within the tolerance, the GPU's (valid) selection replaces
-    the oracle's and that token is recomputed with it."""
-    ref = O.moe_prefill(x64, lw)
-    forced = compare_routing(ref, gpu_ids)
-    y, w = ref["y"].copy(), ref["weights"].copy()
-    for t, sel in forced.items():
-        sub = O.moe_layer(x64[t:t + 1], lw, forced={0: sel})
-        y[t], w[t] = sub["y"][0], sub["weights"][0]
-        lw.drop_cache()
-    lw.drop_cache()
-    return y, w, len(forced)
-
-
-def check_prefill(x, lw, y, ids, w):
-    x64 = bf16_to_f64(x)
-    y_ref, w_ref, n_forced = reference_rows(x64, lw, ids)
-    assert np.allclose(w, w_ref, rtol=1e-6, atol=1e-7)
-    st = check_output(bf16_to_f64(y), y_ref)
-    st["near_ties"] = n_forced
-    return st
 
 
 @pytest.mark.parametrize("T", [1, 9, 300])
