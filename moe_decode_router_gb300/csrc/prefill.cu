@@ -642,6 +642,13 @@ __global__ void __launch_bounds__(G_THREADS, 1) prefill_gemm_kernel(const GemmPa
   tc05::fence_after_sync();
   const uint32_t tmem = *tslot;
   const int n_items = sprefix[NE];
+  // Bounded wait shared by every role.  Where a whole warp waits and then goes
+  // on to warp-synchronous instructions (shuffles, stmatrix, tcgen05.ld), its
+  // lanes agree on the result: the awaited phase cannot move on without a later
+  // arrival of this same warp, so once one lane sees it complete every lane
+  // does, and the time limit is judged on the clock all lanes read in the same
+  // instruction.  (The MMA warp elects among __activemask() and needs no such
+  // argument.)
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (mbar_try_wait(bar, parity)) return true;  // the usual case: one probe
     if (*abort_flag) return false;
