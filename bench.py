@@ -219,6 +219,31 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def prefill_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("moe_decode_router_gb300/csrc/prefill.cu", "moe_decode_router_gb300/csrc/tc05.cuh",
+              "moe_decode_router_gb300/csrc/flint_common.cuh"):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_prefill_traffic(workload: str):
+    """DRAM bytes (read + write) of one prefill sublayer, summed over its kernels, from
+    the committed ncu summary; None if there is none or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "prefill8192_nvfp4_kernels.md")
+    if not os.path.exists(path):
+        return None, None
+    src = prefill_source_hash()
+    for line in open(path):
+        if line.startswith("flint-traffic "):
+            kv = dict(t.split("=", 1) for t in line.split()[1:])
+            if kv.get("workload") == workload and kv.get("source") == src:
+                return int(kv["bytes"]), os.path.relpath(path, ROOT)
+    return None, None
+
+
 def profiled_traffic_ratio(workload: str):
     """DRAM traffic / algorithmic bytes of one sublayer from the committed ncu summary,
     or None if there is none for this workload or the kernels changed since."""
@@ -341,6 +366,7 @@ def run_prefill(args, wl):
     peak = peaks.get("bf16_tflops_sustained")
     peak_src = "measured (sustained bf16 cuBLAS)" if peak else "fallback"
     peak = peak or 1700.0
+    ptraffic, _ = profiled_prefill_traffic(args.workload)
     out = {
         "metric": METRIC,
         "value": round(ms_per_step * 1000.0, 2),
@@ -365,7 +391,7 @@ def run_prefill(args, wl):
             "kernel": "prefill sublayer (router GEMM, routing, grouped gate/up and down GEMMs, combine)",
             "bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(tflops / peak, 4), "peak_source": peak_src,
-            "flops_per_layer": flops, "traffic": None,
+            "flops_per_layer": flops, "traffic": ptraffic,
         },
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": "us/layer",
                 "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": T * 2048 * 2},
