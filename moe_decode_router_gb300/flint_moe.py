@@ -121,6 +121,47 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _expect(t, name, dtype, shape):
+    """Marshalling check of one tensor argument: dtype, shape (None = any length
+    of a 1-D tensor), contiguity, and residence on the current CUDA device.  The
+    C ABI receives bare pointers and cannot check these; a wrong shape would make
+    the kernels read or write outside the tensor."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if shape is None:
+        if t.dim() != 1:
+            raise ValueError(f"{name}: expected a 1-D byte buffer, got shape {tuple(t.shape)}")
+    elif tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if not t.is_cuda or t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: must be on the current CUDA device")
+
+
+def _rows(x, name="x") -> int:
+    """Token count of an activation tensor [rows][HIDDEN]."""
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(x).__name__}")
+    if x.dim() != 2:
+        raise ValueError(f"{name}: expected [tokens][{HIDDEN}], got shape {tuple(x.shape)}")
+    return int(x.shape[0])
+
+
+def _check_io(x, y, topk_ids, topk_w, layers=None):
+    rows = _rows(x)
+    _expect(x, "x", torch.bfloat16, (rows, HIDDEN))
+    _expect(y, "y", torch.bfloat16, (rows, HIDDEN))
+    lead = () if layers is None else (layers,)
+    if topk_ids is not None:
+        _expect(topk_ids, "topk_ids", torch.int32, lead + (rows, TOP_K))
+    if topk_w is not None:
+        _expect(topk_w, "topk_w", torch.float32, lead + (rows, TOP_K))
+    return rows
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -145,6 +186,16 @@ def workspace_bytes(weight_dtype: int = W_NVFP4, max_tokens: int = MAX_DECODE_BA
 
 
 def pack_weights(gate_up, gate_up_scales, down, down_scales, packed, weight_dtype=W_NVFP4, stream=None):
+    ne = N_EXPERTS + N_SHARED
+    if weight_dtype == W_NVFP4:
+        _expect(gate_up, "gate_up", torch.uint8, (ne, 2 * INTER, HIDDEN // 2))
+        _expect(gate_up_scales, "gate_up_scales", torch.uint8, (ne, 2 * INTER, HIDDEN // 16))
+        _expect(down, "down", torch.uint8, (ne, HIDDEN, INTER // 2))
+        _expect(down_scales, "down_scales", torch.uint8, (ne, HIDDEN, INTER // 16))
+    else:
+        _expect(gate_up, "gate_up", torch.bfloat16, (ne, 2 * INTER, HIDDEN))
+        _expect(down, "down", torch.bfloat16, (ne, HIDDEN, INTER))
+    _expect(packed, "packed", torch.uint8, None)
     d = dims(weight_dtype)
     rc = _lib().flint_moe_pack_weights(ctypes.byref(d), _ptr(gate_up), _ptr(gate_up_scales), _ptr(down),
                                        _ptr(down_scales), _ptr(packed), packed.numel() * packed.element_size(),
@@ -163,6 +214,12 @@ class FlintLayer:
         self.weight_dtype = weight_dtype
 
     def c_struct(self) -> Layer:
+        _expect(self.router_w, "router_w", torch.bfloat16, (N_EXPERTS, HIDDEN))
+        _expect(self.experts, "experts", torch.uint8, None)
+        if self.tensor_scales is not None:
+            _expect(self.tensor_scales, "tensor_scales", torch.float32, (N_EXPERTS + N_SHARED, 2))
+        if self.norm_w is not None:
+            _expect(self.norm_w, "norm_w", torch.bfloat16, (HIDDEN,))
         return Layer(_ptr(self.router_w), _ptr(self.experts), _ptr(self.tensor_scales), _ptr(self.norm_w))
 
 
@@ -189,7 +246,8 @@ def pack_layer(plain: dict, device="cuda", stream=None) -> FlintLayer:
 def decode_layer(layer: FlintLayer, x, y, ws, topk_ids=None, topk_w=None, rms_eps=1e-6, stream=None):
     d = dims(layer.weight_dtype, rms_eps)
     L = layer.c_struct()
-    B = x.shape[0]
+    B = _check_io(x, y, topk_ids, topk_w)
+    _expect(ws, "ws", torch.uint8, None)
     rc = _lib().flint_moe_decode_layer(ctypes.byref(d), ctypes.byref(L), _ptr(x), B, _ptr(y), _ptr(topk_ids),
                                        _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "flint_moe_decode_layer")
@@ -203,7 +261,8 @@ def decode_layer_noalloc(layer: FlintLayer, x, y, topk_ids=None, topk_w=None, rm
     """
     d = dims(layer.weight_dtype, rms_eps)
     L = layer.c_struct()
-    rc = _lib().flint_moe_decode_layer_noalloc(ctypes.byref(d), ctypes.byref(L), _ptr(x), x.shape[0], _ptr(y),
+    B = _check_io(x, y, topk_ids, topk_w)
+    rc = _lib().flint_moe_decode_layer_noalloc(ctypes.byref(d), ctypes.byref(L), _ptr(x), B, _ptr(y),
                                                _ptr(topk_ids), _ptr(topk_w), _stream(stream))
     _check(rc, "flint_moe_decode_layer_noalloc")
 
@@ -213,7 +272,11 @@ def decode_stack(layers, x, y, ws, ids_per_layer=None, w_per_layer=None, ys_per_
     fmt = layers[0].weight_dtype
     d = dims(fmt, rms_eps)
     arr = (Layer * len(layers))(*[l.c_struct() for l in layers])
-    rc = _lib().flint_moe_decode_stack(ctypes.byref(d), arr, len(layers), _ptr(x), x.shape[0], _ptr(y),
+    B = _check_io(x, y, ids_per_layer, w_per_layer, layers=len(layers))
+    if ys_per_layer is not None:
+        _expect(ys_per_layer, "ys_per_layer", torch.bfloat16, (len(layers), B, HIDDEN))
+    _expect(ws, "ws", torch.uint8, None)
+    rc = _lib().flint_moe_decode_stack(ctypes.byref(d), arr, len(layers), _ptr(x), B, _ptr(y),
                                        _ptr(ids_per_layer), _ptr(w_per_layer), _ptr(ys_per_layer), _ptr(ws),
                                        ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "flint_moe_decode_stack")
@@ -222,7 +285,9 @@ def decode_stack(layers, x, y, ws, ids_per_layer=None, w_per_layer=None, ys_per_
 def prefill_layer(layer: FlintLayer, x, y, ws, topk_ids=None, topk_w=None, rms_eps=1e-6, stream=None):
     d = dims(layer.weight_dtype, rms_eps)
     L = layer.c_struct()
-    rc = _lib().flint_moe_prefill_layer(ctypes.byref(d), ctypes.byref(L), _ptr(x), x.shape[0], _ptr(y),
+    T = _check_io(x, y, topk_ids, topk_w)
+    _expect(ws, "ws", torch.uint8, None)
+    rc = _lib().flint_moe_prefill_layer(ctypes.byref(d), ctypes.byref(L), _ptr(x), T, _ptr(y),
                                         _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(stream))
     _check(rc, "flint_moe_prefill_layer")
