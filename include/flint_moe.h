@@ -112,7 +112,8 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
 /*
  * One MoE sublayer for a decode batch of 1..8 independent tokens.
  *   x        bf16 [B][H] input (RMSNorm'd first if layer->norm_w != NULL)
- *   y        bf16 [B][H] output; must not alias x
+ *   y        bf16 [B][H] output; must not overlap x (nor either of them the
+ *            workspace: FLINT_MOE_ERR_INVALID_ARG)
  *   topk_ids int32 [B][6] selected experts (descending score) or NULL
  *   topk_w   fp32  [B][6] their renormalised weights, or NULL
  * Three kernels chained with programmatic dependent launch: the router GEMV
@@ -131,7 +132,7 @@ int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *la
  * set; no residual is added).  The chain of 3*n_layers kernels is captured
  * once into a CUDA graph (cached per argument set; see flint_moe_release) and
  * replayed with one graph launch per call.
- *   x, y            bf16 [B][H]; y must not alias x
+ *   x, y            bf16 [B][H]; must not overlap each other or the workspace
  *   ids_per_layer   int32 [n_layers][B][6] or NULL
  *   w_per_layer     fp32  [n_layers][B][6] or NULL
  *   ys_per_layer    bf16  [n_layers][B][H] every sublayer's output, or NULL
@@ -154,7 +155,7 @@ int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *la
  * on the tensor cores (tcgen05, fp32 accumulation), weighted combine plus the
  * shared expert.
  *   x        bf16 [T][H] (RMSNorm'd first if layer->norm_w != NULL)
- *   y        bf16 [T][H]; must not alias x
+ *   y        bf16 [T][H]; must not overlap x (nor either of them the workspace)
  *   topk_ids int32 [T][6] or NULL; topk_w fp32 [T][6] or NULL
  *   ws       flint_moe_workspace_bytes(dims, T) bytes, 256-byte aligned, no
  *            initialisation needed

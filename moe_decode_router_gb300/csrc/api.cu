@@ -88,6 +88,18 @@ int check_layer(const flint_moe_dims* d, const flint_moe_layer* L) {
 
 bool opt_aligned(const void* p) { return p == nullptr || aligned(p, 16); }
 
+// True if the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+// x and y (bf16 [rows][H]) must not overlap each other or the workspace.
+bool io_overlap(const void* x, const void* y, int rows, const void* ws, size_t ws_need) {
+  const size_t act = (size_t)rows * H * 2;
+  return overlap(x, act, y, act) || (ws != nullptr && (overlap(x, act, ws, ws_need) || overlap(y, act, ws, ws_need)));
+}
+
 LayerArgs layer_args(const flint_moe_layer& L) {
   LayerArgs a;
   a.router_w = L.router_w;
@@ -195,6 +207,7 @@ int flint_moe_decode_layer(const flint_moe_dims* dims, const flint_moe_layer* la
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+  if (io_overlap(x, y, B, ws, decode_ws_needed())) return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
@@ -219,6 +232,7 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
       !opt_aligned(w_per_layer) || !opt_aligned(ys_per_layer))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+  if (io_overlap(x, y, B, ws, decode_ws_needed())) return FLINT_MOE_ERR_INVALID_ARG;
 
   std::vector<uintptr_t> key;
   key.reserve(16 + 4 * (size_t)n_layers);
@@ -297,6 +311,7 @@ int flint_moe_decode_layer_noalloc(const flint_moe_dims* dims, const flint_moe_l
   if (x == nullptr || y == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
+  if (io_overlap(x, y, B, nullptr, 0)) return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   NoallocState* ns = nullptr;
   if ((st = noalloc_state(&ns)) != FLINT_MOE_OK) return st;
@@ -318,6 +333,7 @@ int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* l
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < prefill_ws_bytes(T)) return FLINT_MOE_ERR_WORKSPACE;
+  if (io_overlap(x, y, T, ws, prefill_ws_bytes(T))) return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;

@@ -78,6 +78,11 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 8, 0, 1e-6)) == F.FLINT_MOE_ERR_UNSUPPORTED
     assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 6, 7, 1e-6)) == F.FLINT_MOE_ERR_UNSUPPORTED
     assert _decode(lib, d=F.Dims(2048, 256, 1, 512, 6, 0, float("nan"))) == F.FLINT_MOE_ERR_INVALID_ARG
+    # byte ranges: B = 1 activations are 4096 bytes; x, y and the workspace must not share any
+    far = FAKE + (1 << 30)
+    assert _decode(lib, x=FAKE, y=FAKE + 4080, ws=far) == F.FLINT_MOE_ERR_INVALID_ARG    # y overlaps x
+    assert _decode(lib, x=FAKE, y=FAKE + 8192, ws=FAKE + 8192 + 3840) == F.FLINT_MOE_ERR_INVALID_ARG  # ws overlaps y
+    assert _decode(lib, x=far + 4096, y=FAKE, ws=far) == F.FLINT_MOE_ERR_INVALID_ARG     # ws overlaps x
 
 
 def test_stack_and_pack_reject_bad_arguments_on_host(lib):
@@ -131,3 +136,7 @@ def test_prefill_rejects_bad_arguments_on_host(lib):
     assert call(x=FAKE + 1032) == F.FLINT_MOE_ERR_INVALID_ARG
     assert call(ws=FAKE + 4112) == F.FLINT_MOE_ERR_INVALID_ARG
     assert call(L=_layer(tensor_scales=None)) == F.FLINT_MOE_ERR_INVALID_ARG
+    act = 8192 * 2048 * 2
+    far = FAKE + (1 << 36)
+    assert call(x=FAKE, y=FAKE + act - 16, ws=far) == F.FLINT_MOE_ERR_INVALID_ARG       # y overlaps x
+    assert call(x=FAKE, y=FAKE + act, ws=FAKE + 2 * act - 256) == F.FLINT_MOE_ERR_INVALID_ARG  # ws overlaps y
