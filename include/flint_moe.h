@@ -43,7 +43,8 @@ typedef struct CUstream_st *flint_moe_stream_t;
 /* Status codes returned by every int-returning entry point. */
 enum {
     FLINT_MOE_OK = 0,
-    FLINT_MOE_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad count  */
+    FLINT_MOE_ERR_INVALID_ARG = -1, /* null, misaligned or overlapping
+                                       buffers, bad count                   */
     FLINT_MOE_ERR_UNSUPPORTED = -2, /* shape or batch outside the fast path */
     FLINT_MOE_ERR_WORKSPACE = -3,   /* workspace or output buffer too small */
     FLINT_MOE_ERR_CUDA = -4,        /* a CUDA runtime call failed           */
