@@ -18,10 +18,13 @@ full-history KV"):
     the reference rounding).
 
 The pages do not print the rounding points.  This oracle declares them
-(readings, listed in the design notes): dot products accumulate exactly (fp64
-here) and are rounded once to fp32; bf16 rounding (round-to-nearest-even, via
-fp32) after the RMSNorm, after the router logits, after SiLU(gate)*up and
-after the weighted combine.  Routing weights are the selected sigmoid scores
+(readings, listed in the design notes): dot products accumulate exactly and
+are rounded once to fp32; bf16 rounding (round-to-nearest-even, via fp32)
+after the RMSNorm, after the router logits, after SiLU(gate)*up and after the
+weighted combine.  Where a rounded sum decides an integer result (the router
+logits that feed top-6, the RMSNorm scale) the oracle rounds the exact sum
+itself (``round_sum_f32``); the expert GEMVs, whose results are only compared
+within a tolerance, sum in fp64 before the one fp32 rounding.  Routing weights are the selected sigmoid scores
 divided by their sum; the shared expert is added with weight 1; there is no
 residual inside the sublayer.
 
@@ -39,7 +42,7 @@ import numpy as np
 __all__ = [
     "H", "E", "INTER", "TOP_K", "BLOCK", "RMS_EPS",
     "e2m1_value", "e4m3fn_value", "E2M1_LUT", "E4M3_LUT",
-    "bf16_bits_to_f64", "round_f32", "round_bf16", "f64_to_bf16_bits",
+    "bf16_bits_to_f64", "round_f32", "round_bf16", "f64_to_bf16_bits", "round_sum_f32",
     "dequant_nvfp4", "rmsnorm", "router_logits", "sigmoid_scores",
     "topk_desc", "route", "silu_mul", "expert_gate_up", "expert_down",
     "LayerView", "layer_from_tensors", "moe_layer", "moe_stack", "moe_prefill",
@@ -120,6 +123,35 @@ def round_bf16(x):
     return bf16_bits_to_f64(f64_to_bf16_bits(x))
 
 
+def round_sum_f32(terms):
+    """The fp32 value nearest the exact sum of `terms` (float64 values), ties to even.
+
+    math.fsum gives d, the float64 nearest the exact sum S.  Rounding d to fp32
+    gives the fp32 nearest S except where d is exactly halfway between two fp32
+    values while S is not (double rounding): S < m implies d <= m for every
+    fp32 midpoint m, since m is itself a float64.  In that case the sign of the
+    exact residual S - d (fsum of the terms and -d, whose sign is exact) picks
+    the side.
+    """
+    terms = [float(t) for t in np.ravel(terms)]
+    d = math.fsum(terms)
+    f = np.float32(d)
+    if float(f) == d or not np.isfinite(f):
+        return float(f)
+    if float(f) < d:
+        lo, hi = f, np.nextafter(f, np.float32(np.inf))
+    else:
+        lo, hi = np.nextafter(f, np.float32(-np.inf)), f
+    if d - float(lo) != float(hi) - d:
+        return float(f)
+    r = math.fsum(terms + [-d])
+    if r > 0:
+        return float(hi)
+    if r < 0:
+        return float(lo)
+    return float(f)
+
+
 # ----------------------------------------------------------------------------
 # NVFP4 dequantisation
 # ----------------------------------------------------------------------------
@@ -156,7 +188,8 @@ def rmsnorm(y, w, eps=RMS_EPS):
     y [B, H] and w [H] hold bf16 values as float64.
     """
     y = np.atleast_2d(np.asarray(y, dtype=np.float64))
-    ss = np.array([math.fsum(row * row) for row in y])  # exact sum of exact squares
+    # the exact sum of the exact squares, rounded once to fp32; / H is exact (H = 2^11)
+    ss = np.array([round_sum_f32(row * row) for row in y])
     ms = (ss / y.shape[-1]).astype(np.float32)
     r = np.float32(1.0) / np.sqrt(ms + np.float32(eps))
     t = y.astype(np.float32) * r[:, None]
@@ -165,8 +198,27 @@ def rmsnorm(y, w, eps=RMS_EPS):
 
 
 def router_logits(xh, router_w):
-    """Router GEMV over the 256 experts: logit = bf16(fp32(sum_k x_hat[k] * W_r[e, k]))."""
-    return round_bf16(round_f32(np.asarray(xh, np.float64) @ np.asarray(router_w, np.float64).T))
+    """Router GEMV over the 256 experts: logit = bf16(fp32(sum_k x_hat[k] * W_r[e, k])),
+    the sum exact before its one rounding to fp32.
+
+    Products of bf16 values are exact in float64.  A float64 matrix product
+    approximates each sum S within gamma * sum|products| for any summation
+    order (gamma = n * 2^-53 / (1 - n * 2^-53), taken here as (n + 2) * 2^-52);
+    where every value of that interval rounds to the same fp32, that fp32 is
+    the rounding of S.  The few sums whose interval holds an fp32 rounding
+    boundary are rounded exactly with ``round_sum_f32``.
+    """
+    xh = np.atleast_2d(np.asarray(xh, np.float64))
+    w = np.asarray(router_w, np.float64)
+    approx = xh @ w.T
+    bound = (np.abs(xh) @ np.abs(w).T) * ((xh.shape[1] + 2) * 2.0 ** -52)
+    with np.errstate(over="ignore"):
+        lo = (approx - bound).astype(np.float32)
+        hi = (approx + bound).astype(np.float32)
+    out = lo.astype(np.float64)
+    for t, e in zip(*np.nonzero(lo != hi)):
+        out[t, e] = round_sum_f32(xh[t] * w[e])
+    return round_bf16(out)
 
 
 def sigmoid_scores(logits):

@@ -109,6 +109,86 @@ def test_round_f32_is_nearest_even():
     assert O.round_f32(one + 0.51 * ulp) == one + ulp
 
 
+def _exact_round_to_f32(q):
+    """Nearest fp32 (ties to even) of a rational, by exact integer arithmetic."""
+    from fractions import Fraction
+    if q == 0:
+        return 0.0
+    sign = -1.0 if q < 0 else 1.0
+    a = abs(Fraction(q))
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)                       # subnormals share the smallest exponent's spacing
+    scaled = a / Fraction(2) ** (e - 23)   # significand with 23 fraction bits
+    m, rem = divmod(scaled.numerator, scaled.denominator)
+    twice = 2 * rem
+    if twice > scaled.denominator or (twice == scaled.denominator and m % 2 == 1):
+        m += 1
+    return sign * float(Fraction(m) * Fraction(2) ** (e - 23))
+
+
+def test_round_sum_f32_equals_exact_rational_rounding():
+    from fractions import Fraction
+    rng = np.random.default_rng(12)
+    cases = []
+    # a sum whose float64 rounding lands on an fp32 midpoint: fsum alone would tie to even
+    cases.append([1.0, 2.0 ** -8, 2.0 ** -24, 2.0 ** -60])
+    cases.append([1.0, 2.0 ** -8, 2.0 ** -24, -(2.0 ** -60)])
+    cases.append([1.0, 2.0 ** -24])                     # an exact midpoint: ties to even
+    cases.append([1.0, 3 * 2.0 ** -24])                 # an exact midpoint, odd side
+    cases.append([2.0 ** 60, 1.0, -(2.0 ** 60)])        # cancellation
+    cases.append([1e-45, 1e-46])                        # fp32 subnormal range
+    for _ in range(300):
+        n = int(rng.integers(2, 40))
+        t = O.round_bf16(rng.standard_normal(n)) * O.round_bf16(rng.standard_normal(n))
+        t *= np.exp2(rng.integers(-30, 30, size=n))
+        cases.append(list(t))
+    for _ in range(300):  # sums placed on an fp32 midpoint, nudged by a tiny term either way
+        base = float(np.float32(rng.standard_normal()))
+        ulp = float(np.spacing(np.float32(base)))
+        tiny = float(rng.choice([-1.0, 0.0, 1.0])) * abs(base) * 2.0 ** -70
+        cases.append([base, ulp / 2, tiny])
+    for terms in cases:
+        want = _exact_round_to_f32(sum(Fraction(x) for x in terms))
+        got = O.round_sum_f32(terms)
+        assert got == want, (terms, got, want)
+
+
+def test_router_logits_round_the_exact_sum_not_a_float64_sum():
+    """logit = bf16(fp32(S)) of the exact sum S = 1 + 2^-8 + 2^-24 + 2^-60.  fp32(S) is
+    1 + 2^-8 + 2^-23 (S is just above the fp32 midpoint 1 + 2^-8 + 2^-24), whose bf16
+    rounding is 1 + 2^-7.  A float64 sum loses the 2^-60 term, lands on the midpoint,
+    ties to 1 + 2^-8 in fp32 and to 1.0 in bf16."""
+    x = np.array([[1.0, 2.0 ** -8, 2.0 ** -24, 2.0 ** -60]])
+    W = np.ones((1, 4))
+    assert O.router_logits(x, W)[0, 0] == 1.0 + 2.0 ** -7
+    naive = O.round_bf16(O.round_f32(((1.0 + 2.0 ** -8) + 2.0 ** -24) + 2.0 ** -60))
+    assert naive == 1.0  # the pin separates the exact definition from a float64 sum
+    # the same terms spread over 2048 columns and 3 experts, in another order
+    big = np.zeros((2, 2048))
+    big[0, [5, 700, 1500, 2047]] = [2.0 ** -60, 2.0 ** -24, 1.0, 2.0 ** -8]
+    big[1, 0] = 3.0
+    Wb = np.zeros((3, 2048))
+    Wb[1, :] = 1.0
+    Wb[2, 0] = 2.0
+    got = O.router_logits(big, Wb)
+    assert got[0, 1] == 1.0 + 2.0 ** -7 and got[0, 0] == 0.0 and got[0, 2] == 0.0
+    assert got[1, 1] == 3.0 and got[1, 2] == 6.0
+
+
+def test_router_logits_match_exact_rounding_on_random_rows():
+    from fractions import Fraction
+    rng = np.random.default_rng(13)
+    xh = O.round_bf16(rng.standard_normal((3, 256)))
+    W = O.round_bf16(rng.standard_normal((8, 256)) / 16)
+    got = O.router_logits(xh, W)
+    for t in range(3):
+        for e in range(8):
+            s = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(xh[t], W[e]))
+            assert got[t, e] == O.round_bf16(_exact_round_to_f32(s))
+
+
 # --------------------------------------------------------------------------- GEMV special cases
 
 def _int_nvfp4(rng, n, k):
