@@ -1,31 +1,38 @@
 """Benchmark of the Flint MoE decode step on GB300: us per MoE sublayer and effective HBM GB/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                    [--no-extras] [--no-cpu-baseline]
 
 Workloads (weights drawn on the GPU by the seeded generator, 47 distinct sublayers):
   stack47_b1_nvfp4   47 chained NVFP4 sublayers, batch 1     (default)
   stack47_b8_nvfp4   same weights, batch 8
   stack47_b8_bf16    47 chained BF16-expert sublayers, batch 8 (~76 GB)
   prefill8192_nvfp4  one NVFP4 sublayer over 8,192 tokens (tensor-core grouped GEMMs)
-A step is one pass of the 47-sublayer stack (one CUDA-graph launch of 141
-kernels) over one batch; inputs cycle through 16 seeded batches so routing,
-and hence the experts touched, changes every step.  The resident weights
-(21.4 GB NVFP4 / 76 GB BF16) and the bytes touched per step (>= 631 MB) are far
-larger than the 129 MB L2, so weights stream from HBM.
+A step is one pass of the 47-sublayer stack over one batch (NVFP4: one
+launch of the persistent decode kernel; BF16: one CUDA-graph launch of 141
+kernels); inputs cycle through 16 seeded batches so routing, and hence the
+experts touched, changes every step.  The resident weights (21.4 GB NVFP4 /
+76 GB BF16) and the bytes touched per step (>= 631 MB) are far larger than the
+129 MB L2, so weights stream from HBM.
 
 The JSON line reports `value` = us per sublayer (lower is better) measured with
 CUDA events over K steps, the algorithmic HBM bytes of the step (router +
 shared + distinct selected experts, counted from the actual routing), the
-roofline fraction of the decode sublayer against the measured HBM copy
-bandwidth, the end-to-end number through the C ABI with host buffers, SM
-clocks sampled during the timed region, and the CPU oracle timed on a bounded
-sample (`cpu_baseline`).  `--impl reference` times only the oracle.
+roofline fraction against the measured HBM copy bandwidth, the end-to-end
+number through the C ABI with host buffers, SM clocks sampled during the timed
+region, and the CPU oracle timed on a bounded sample (`cpu_baseline`: all host
+cores, one independent oracle process per core; `single_core` inside it).
+The default run also measures batch 8, the prefill sublayer and the BF16
+batch-8 stack and reports each under its own key of the same line
+(`--no-extras` skips them).  `--impl reference` times only the oracle, on the
+same workload and with the same `config`.
 """
 
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -41,6 +48,7 @@ NVFP4_EXPERT_BYTES = 1_769_472
 BF16_EXPERT_BYTES = 6_291_456
 ROUTER_BYTES = 256 * 2048 * 2
 N_INPUTS = 16
+FUSED_MAX_LAYERS = 64  # sublayers per launch of the persistent NVFP4 decode kernel
 
 WORKLOADS = {
     "stack47_b1_nvfp4": dict(cfg=1, batch=1, fmt="nvfp4"),
@@ -54,13 +62,14 @@ METRIC = "MoE decode µs/layer & effective HBM GB/s (% of roofline) at batch 1 a
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--layers", type=int, default=N_LAYERS,
                     help="sublayers in the stack (47 for the benchmark; fewer only for profiling captures)")
     ap.add_argument("--workload", default="stack47_b1_nvfp4", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="measure only --workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -72,6 +81,25 @@ def dist_env():
     return world, rank, local
 
 
+def workload_config(name: str, world: int, layers: int = N_LAYERS) -> dict:
+    """The `config` object of a workload; both arms print exactly this."""
+    wl = WORKLOADS[name]
+    if wl.get("prefill"):
+        return {"workload": name, "tokens": wl["batch"], "hidden": 2048, "experts": "256+1", "inter": 512,
+                "top_k": 6, "weights": wl["fmt"], "parallelism": f"replicas x{world}",
+                "l2": "every step streams all 257 experts' packed weights (455 MB) and 4 rotating 32 MB token "
+                      "batches: far larger than L2"}
+    return {"workload": name, "layers": layers, "batch": wl["batch"], "hidden": 2048, "experts": "256+1",
+            "inter": 512, "top_k": 6, "weights": wl["fmt"], "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2: 16 rotating batches, >= 631 MB of weights touched per step out of "
+                  f"{'21.4' if wl['fmt'] == 'nvfp4' else '76'} GB resident"}
+
+
+def read_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    return json.load(open(path)) if os.path.exists(path) else {}
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 _ORACLE_CHILD = r"""
@@ -80,24 +108,70 @@ sys.path.insert(0, os.environ["FLINT_ROOT"])
 import numpy as np, torch
 torch.set_num_threads(1)
 import oracle as O, synth
-cfg, batch, budget, fmt = int(sys.argv[1]), int(sys.argv[2]), float(sys.argv[3]), sys.argv[4]
-layers = [synth.gen_layer(cfg, i, device="cpu") for i in (1, 2)]
-lws = [O.layer_from_tensors(d) for d in layers]
-del layers
-x = synth.gen_x(cfg, batch, index=0)
+cfg, batch, budget, seed_index = int(sys.argv[1]), int(sys.argv[2]), float(sys.argv[3]), int(sys.argv[4])
+lw = O.layer_from_tensors(synth.gen_layer(cfg, 1, device="cpu"))
+x = synth.gen_x(cfg, batch, index=seed_index)
 y = O.bf16_bits_to_f64(x.view(torch.int16).numpy().view(np.uint16))
+print("ready", flush=True)
+sys.stdin.readline()
 n = 0
 t0 = time.perf_counter()
 while True:
-    lw = lws[n % 2]
     lw.drop_cache()
     y = O.moe_layer(y, lw)["y"]
     n += 1
     if time.perf_counter() - t0 >= budget and n >= 2:
         break
 dt = time.perf_counter() - t0
-print(json.dumps({"layers": n, "seconds": dt}))
+print(json.dumps({"layers": n, "seconds": dt}), flush=True)
 """
+
+
+def time_oracle(cfg: int, batch: int, fmt: str, budget_s: float, procs: int = 1) -> dict:
+    """The oracle on a bounded sample: `procs` independent single-threaded processes, each
+    chaining sublayers (the same seeded weights, its own input) for `budget_s` seconds after
+    all are ready.  Returns the aggregate throughput as us per sublayer."""
+    env = dict(os.environ)
+    env.update(FLINT_ROOT=ROOT, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    kids = [subprocess.Popen([sys.executable, "-c", _ORACLE_CHILD, str(cfg), str(batch), str(budget_s), str(i)],
+                             stdin=subprocess.PIPE, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                             env=env) for i in range(procs)]
+    try:
+        for k in kids:
+            line = k.stdout.readline()
+            if line.strip() != "ready":
+                raise RuntimeError(f"oracle child failed: {k.stderr.read()[-2000:]}")
+        for k in kids:  # start together
+            k.stdin.write("go\n")
+            k.stdin.flush()
+        res = []
+        for k in kids:
+            out, err = k.communicate(timeout=900)
+            if k.returncode != 0:
+                raise RuntimeError(f"oracle child failed: {err[-2000:]}")
+            res.append(json.loads(out.strip().splitlines()[-1]))
+    finally:
+        for k in kids:
+            if k.poll() is None:
+                k.kill()
+    rate = sum(r["layers"] / r["seconds"] for r in res)  # sublayers per second, all processes together
+    n = sum(r["layers"] for r in res)
+    secs = max(r["seconds"] for r in res)
+    return dict(value=1e6 / rate, unit="us/layer", cores=procs, kind="oracle",
+                sample=f"{n} sublayers of the {fmt} stack at batch {batch} in {procs} independent "
+                       f"single-threaded numpy fp64 process{'es' if procs > 1 else ''} over {secs:.1f} s")
+
+
+def time_oracle_all(cfg: int, batch: int, fmt: str, budget_s: float) -> dict:
+    """All host cores (one oracle process per core), with the single-core figure inside."""
+    one = time_oracle(cfg, batch, fmt, budget_s, 1)
+    cores = max(1, min(os.cpu_count() or 1, 64))
+    if cores == 1:
+        return one
+    allc = time_oracle(cfg, batch, fmt, budget_s, cores)
+    allc["single_core"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
+    return allc
 
 
 _ORACLE_PREFILL_CHILD = r"""
@@ -142,24 +216,6 @@ def time_oracle_prefill(cfg: int, tokens: int, small: int = 64, large: int = 256
                        f"evaluated at {tokens} tokens")
 
 
-def time_oracle(cfg: int, batch: int, fmt: str, budget_s: float) -> dict:
-    """Runs the oracle single-threaded in a fresh process on a bounded sample:
-    consecutive sublayers (drawn on the CPU with the same distributions) until
-    `budget_s` seconds of work; returns us per sublayer."""
-    env = dict(os.environ)
-    env.update(FLINT_ROOT=ROOT, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, str(cfg), str(batch), str(budget_s), fmt],
-                       capture_output=True, text=True, env=env, timeout=900)
-    if r.returncode != 0:
-        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
-    res = json.loads(r.stdout.strip().splitlines()[-1])
-    us = res["seconds"] / res["layers"] * 1e6
-    return dict(value=us, unit="us/layer", cores=1, kind="oracle",
-                sample=f"{res['layers']} sublayers of the {fmt} stack at batch {batch}, "
-                       f"{res['seconds']:.1f} s single-threaded numpy fp64 on the host")
-
-
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -181,6 +237,7 @@ class ClockSampler:
                  "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        time.sleep(0.3)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -210,59 +267,47 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- ncu traffic
 
-def kernel_source_hash() -> str:
+def _hash_files(files) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("moe_decode_router_gb300/csrc/decode.cu", "moe_decode_router_gb300/csrc/flint_common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def prefill_source_hash() -> str:
-    import hashlib
-    h = hashlib.sha256()
-    for f in ("moe_decode_router_gb300/csrc/prefill.cu", "moe_decode_router_gb300/csrc/tc05.cuh",
-              "moe_decode_router_gb300/csrc/flint_common.cuh"):
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
+CSRC = "moe_decode_router_gb300/csrc/"
+SOURCES = {
+    "fused": [CSRC + "decode_fused.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
+    "chain": [CSRC + "decode.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
+    "prefill": [CSRC + "prefill.cu", CSRC + "tc05.cuh", CSRC + "flint_common.cuh"],
+}
+TRAFFIC_FILES = {
+    "fused": "profiles/decode_fused_stack_b1_b8.md",
+    "chain": "profiles/decode_chain_bf16_b8.md",
+    "prefill": "profiles/prefill8192_nvfp4_kernels.md",
+}
 
 
-def profiled_prefill_traffic(workload: str):
-    """DRAM bytes (read + write) of one prefill sublayer, summed over its kernels, from
-    the committed ncu summary; None if there is none or the kernels changed since."""
-    path = os.path.join(ROOT, "profiles", "prefill8192_nvfp4_kernels.md")
+def profiled_traffic(kind: str, workload: str):
+    """DRAM bytes per sublayer (read + write) from the committed ncu summary of this
+    path, as a ratio to the algorithmic bytes (decode) or as bytes (prefill); None if
+    there is none for this workload or the kernel sources changed since."""
+    path = os.path.join(ROOT, TRAFFIC_FILES[kind])
     if not os.path.exists(path):
         return None, None
-    src = prefill_source_hash()
+    src = _hash_files(SOURCES[kind])
     for line in open(path):
         if line.startswith("flint-traffic "):
             kv = dict(t.split("=", 1) for t in line.split()[1:])
             if kv.get("workload") == workload and kv.get("source") == src:
-                return int(kv["bytes"]), os.path.relpath(path, ROOT)
-    return None, None
-
-
-def profiled_traffic_ratio(workload: str):
-    """DRAM traffic / algorithmic bytes of one sublayer from the committed ncu summary,
-    or None if there is none for this workload or the kernels changed since."""
-    path = os.path.join(ROOT, "profiles", "decode_kernels_full_b1_b8.md")
-    if not os.path.exists(path):
-        return None, None
-    src = kernel_source_hash()
-    for line in open(path):
-        if line.startswith("flint-traffic "):
-            kv = dict(t.split("=", 1) for t in line.split()[1:])
-            if kv.get("workload") == workload and kv.get("source") == src:
-                return float(kv["ratio"]), os.path.relpath(path, ROOT)
+                return kv, TRAFFIC_FILES[kind]
     return None, None
 
 
 # ----------------------------------------------------------------------------- our arm
 
-def build_stack(F, synth, torch, wl, dev, n_layers):
-    fmt = wl["fmt"]
+def build_stack(F, synth, torch, fmt: str, dev, n_layers: int):
     cfg = 1 if fmt == "nvfp4" else 3  # the NVFP4 stacks share one weight set (config-1 seeds)
     layers = []
     for i in range(n_layers):
@@ -276,6 +321,124 @@ def build_stack(F, synth, torch, wl, dev, n_layers):
     return layers
 
 
+def timed(torch, stream, fn, steps: int) -> float:
+    """Device milliseconds of `steps` calls of fn(s), CUDA events on `stream`."""
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(steps):
+        fn(s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def max_over_ranks(torch, ms: float, world: int, dev) -> float:
+    if world == 1:
+        return ms
+    import torch.distributed as tdist
+    t = torch.tensor([ms], device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+
+
+def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, world: int, dev, local: int) -> dict:
+    """One decode-stack workload: device time, algorithmic bytes, roofline, e2e, clocks."""
+    wl = WORKLOADS[name]
+    B = wl["batch"]
+    fmt = F.W_NVFP4 if wl["fmt"] == "nvfp4" else F.W_BF16
+    NL = len(layers)
+    xs = [synth.gen_x(wl["cfg"], B, index=i, device=dev) for i in range(N_INPUTS)]
+    ys = [torch.empty_like(x) for x in xs]
+    ws = F.alloc_workspace(fmt, B, device=dev)
+
+    # Algorithmic bytes per input: router + (distinct routed + shared) experts per sublayer.
+    expert_bytes = NVFP4_EXPERT_BYTES if fmt == F.W_NVFP4 else BF16_EXPERT_BYTES
+    ids = torch.empty((NL, B, 6), dtype=torch.int32, device=dev)
+    bytes_per_input, uniq = [], []
+    for i, x in enumerate(xs):
+        F.decode_stack(layers, x, ys[i], ws, ids_per_layer=ids)
+        torch.cuda.synchronize()
+        idc = ids.cpu()
+        u = [len(set(idc[l].flatten().tolist())) for l in range(NL)]
+        uniq.extend(u)
+        bytes_per_input.append(sum(ROUTER_BYTES + (n + 1) * expert_bytes for n in u))
+    for i, x in enumerate(xs):  # BF16: one cached graph per input buffer (graphs bake in pointers)
+        F.decode_stack(layers, x, ys[i], ws)
+    torch.cuda.synchronize()
+    assert F.device_error() == 0
+
+    stream = torch.cuda.current_stream()
+    for s in range(max(3, warmup)):
+        F.decode_stack(layers, xs[s % N_INPUTS], ys[s % N_INPUTS], ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    ms = timed(torch, stream, lambda s: F.decode_stack(layers, xs[s % N_INPUTS], ys[s % N_INPUTS], ws), steps)
+    barrier(world)
+    clk = clocks.stop()
+    err = F.device_error()
+
+    # End to end through the C ABI: pinned host input -> device, stack, device -> pinned host.
+    hx = [x.cpu().pin_memory() for x in xs]
+    hy = torch.empty_like(hx[0]).pin_memory()
+    xin = torch.empty_like(xs[0])
+    yout = torch.empty_like(xs[0])
+
+    def e2e_step(s):
+        xin.copy_(hx[s % N_INPUTS], non_blocking=True)
+        F.decode_stack(layers, xin, yout, ws)
+        hy.copy_(yout, non_blocking=True)
+
+    for s in range(max(3, warmup)):
+        e2e_step(s)
+    e2e_steps = max(10, steps // 2)
+    e2e_ms = timed(torch, stream, e2e_step, e2e_steps) / e2e_steps
+
+    ms = max_over_ranks(torch, ms, world, dev)
+    ms_per_step = ms / steps
+    total_bytes = sum(bytes_per_input[s % N_INPUTS] for s in range(steps))
+    gbs = total_bytes * world / (ms / 1000.0) / 1e9
+    peaks = read_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"
+    peak = peak or 6800.0
+    bytes_per_layer = total_bytes / steps / NL
+    kind = "fused" if fmt == F.W_NVFP4 else "chain"
+    prof, prof_src = profiled_traffic(kind, name)
+    traffic = round(float(prof["ratio"]) * bytes_per_layer * NL) if prof else None
+    launches = math.ceil(NL / FUSED_MAX_LAYERS) if fmt == F.W_NVFP4 else 3 * NL
+    return {
+        "value": round(ms_per_step * 1000.0 / NL, 3),
+        "unit": "us/layer",
+        "ms_per_step": round(ms_per_step, 4),
+        "effective_hbm_gbs": round(gbs, 1),
+        "roofline": {
+            "kernel": ("decode_fused_kernel: one persistent launch = the whole 47-sublayer step"
+                       if fmt == F.W_NVFP4 else
+                       "decode step (router + gate/up + down per sublayer, PDL-chained, one CUDA graph)"),
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "peak_source": peak_src,
+            "bytes_per_step": round(total_bytes / steps), "bytes_per_layer": round(bytes_per_layer),
+            "traffic": traffic, "traffic_source": prof_src,
+        },
+        "e2e": {"value": round(e2e_ms * 1000.0 / NL, 3), "unit": "us/layer",
+                "h2d_bytes_per_step": B * 2048 * 2, "d2h_bytes_per_step": B * 2048 * 2},
+        "gpu_launches": steps * launches,
+        "mean_unique_experts_per_layer": round(sum(uniq) / len(uniq), 2),
+        "clocks": clk,
+        "device_error_word": err,
+    }
+
+
 def prefill_flops(T: int) -> float:
     """Algorithmic FLOPs of one prefill sublayer: router GEMM plus gate/up and
     down GEMMs over the 6 T routed and T shared token-expert pairs."""
@@ -283,19 +446,8 @@ def prefill_flops(T: int) -> float:
     return 2.0 * T * E * H + 2.0 * 7 * T * (2 * I * H + H * I)
 
 
-def run_prefill(args, wl):
-    import torch
-    import torch.distributed as tdist
-
-    import synth
-    from moe_decode_router_gb300 import flint_moe as F
-
-    world, rank, local = dist_env()
-    if world > 1:
-        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    F.load_library()
+def measure_prefill(F, synth, torch, name: str, steps: int, warmup: int, world: int, dev, local: int) -> dict:
+    wl = WORKLOADS[name]
     T = wl["batch"]
     plain = synth.gen_layer(wl["cfg"], 0, device=dev)
     L = F.pack_layer(plain, device=dev)
@@ -306,92 +458,51 @@ def run_prefill(args, wl):
     xs = [synth.gen_x(wl["cfg"], T, index=i, device=dev) for i in range(n_in)]
     ys = [torch.empty_like(x) for x in xs]
     ws = F.alloc_workspace(F.W_NVFP4, T, device=dev)
-    for s in range(max(3, args.warmup)):
+    for s in range(max(3, warmup)):
         F.prefill_layer(L, xs[s % n_in], ys[s % n_in], ws)
     torch.cuda.synchronize()
     assert F.device_error() == 0
-    steps = args.steps
     stream = torch.cuda.current_stream()
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        tdist.barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for s in range(steps):
-        F.prefill_layer(L, xs[s % n_in], ys[s % n_in], ws)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tdist.barrier()
+    barrier(world)
+    ms = timed(torch, stream, lambda s: F.prefill_layer(L, xs[s % n_in], ys[s % n_in], ws), steps)
+    barrier(world)
     clk = clocks.stop()
     err = F.device_error()
 
-    # End to end through the C ABI: pinned host tokens -> device, sublayer, device -> pinned host.
     hx = [x.cpu().pin_memory() for x in xs]
     hy = torch.empty_like(hx[0]).pin_memory()
     xin = torch.empty_like(xs[0])
     yout = torch.empty_like(xs[0])
-    for s in range(3):
-        xin.copy_(hx[s % n_in], non_blocking=True)
-        F.prefill_layer(L, xin, yout, ws)
-        hy.copy_(yout, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_steps = max(10, steps // 4)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(e2e_steps):
-        xin.copy_(hx[s % n_in], non_blocking=True)
-        F.prefill_layer(L, xin, yout, ws)
-        hy.copy_(yout, non_blocking=True)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = t0.elapsed_time(t1) / e2e_steps
 
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        tdist.all_reduce(ms_t, op=tdist.ReduceOp.MAX)
-    ms_per_step = float(ms_t.item()) / steps
+    def e2e_step(s):
+        xin.copy_(hx[s % n_in], non_blocking=True)
+        F.prefill_layer(L, xin, yout, ws)
+        hy.copy_(yout, non_blocking=True)
+
+    for s in range(3):
+        e2e_step(s)
+    e2e_steps = max(10, steps // 4)
+    e2e_ms = timed(torch, stream, e2e_step, e2e_steps) / e2e_steps
+
+    ms_per_step = max_over_ranks(torch, ms, world, dev) / steps
     flops = prefill_flops(T)
-    tflops = flops / (ms_per_step / 1000.0) / 1e12
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        peaks = json.load(open(pk_path))
-    peak = peaks.get("bf16_tflops_sustained")
-    peak_src = "measured (sustained bf16 cuBLAS)" if peak else "fallback"
+    tflops = flops * world / (ms_per_step / 1000.0) / 1e12
+    peak = read_peaks().get("bf16_tflops_sustained")
+    peak_src = "measured (MEASURED_PEAKS.json bf16_tflops_sustained)" if peak else "fallback"
     peak = peak or 1700.0
-    ptraffic, _ = profiled_prefill_traffic(args.workload)
-    out = {
-        "metric": METRIC,
+    prof, prof_src = profiled_traffic("prefill", name)
+    return {
         "value": round(ms_per_step * 1000.0, 2),
         "unit": "us/layer",
-        "n_gpus": world,
-        "steps": steps,
-        "warmup": max(3, args.warmup),
         "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": False,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "nvfp4-w/bf16-a (f16/bf16 tensor-core operands, f32 accumulate)",
-        "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
-        "config": {
-            "workload": args.workload, "tokens": T, "hidden": 2048, "experts": "256+1", "inter": 512,
-            "top_k": 6, "weights": "nvfp4", "parallelism": f"replicas x{world}",
-            "l2": "every step streams all 257 experts' packed weights (455 MB) and 4 rotating 32 MB token "
-                  "batches: far larger than L2",
-        },
         "tflops": round(tflops, 1),
         "roofline": {
             "kernel": "prefill sublayer (router GEMM, routing, grouped gate/up and down GEMMs, combine)",
             "bound": "tensor", "achieved": round(tflops, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(tflops / peak, 4), "peak_source": peak_src,
-            "flops_per_layer": flops, "traffic": ptraffic,
+            "flops_per_layer": flops, "traffic": int(prof["bytes"]) if prof else None, "traffic_source": prof_src,
         },
         "e2e": {"value": round(e2e_ms * 1000.0, 2), "unit": "us/layer",
                 "h2d_bytes_per_step": T * 2048 * 2, "d2h_bytes_per_step": T * 2048 * 2},
@@ -399,20 +510,13 @@ def run_prefill(args, wl):
         "clocks": clk,
         "device_error_word": err,
     }
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
-        try:
-            out["cpu_baseline"] = time_oracle_prefill(wl["cfg"], T)
-        except Exception as e:  # report, do not hide
-            out["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        tdist.destroy_process_group()
+
+
+def dtype_of(fmt: str) -> str:
+    return {"nvfp4": "nvfp4-w/bf16-a (f16 operands, f32 accumulate)", "bf16": "bf16 (f32 accumulate)"}[fmt]
 
 
 def run_ours(args):
-    if WORKLOADS[args.workload].get("prefill"):
-        return run_prefill(args, WORKLOADS[args.workload])
     import torch
     import torch.distributed as tdist
 
@@ -425,141 +529,74 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     F.load_library()
-    wl = WORKLOADS[args.workload]
-    B = wl["batch"]
-    fmt = F.W_NVFP4 if wl["fmt"] == "nvfp4" else F.W_BF16
-    NL = args.layers
-    layers = build_stack(F, synth, torch, wl, dev, NL)
-    xs = [synth.gen_x(wl["cfg"], B, index=i, device=dev) for i in range(N_INPUTS)]
-    ys = [torch.empty_like(x) for x in xs]
-    ws = F.alloc_workspace(fmt, B, device=dev)
+    name = args.workload
+    wl = WORKLOADS[name]
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
 
-    # Algorithmic bytes per input: router + (distinct routed + shared) experts per sublayer.
-    expert_bytes = NVFP4_EXPERT_BYTES if fmt == F.W_NVFP4 else BF16_EXPERT_BYTES
-    ids = torch.empty((NL, B, 6), dtype=torch.int32, device=dev)
-    bytes_per_input = []
-    uniq = []
-    for i, x in enumerate(xs):
-        F.decode_stack(layers, x, ys[i], ws, ids_per_layer=ids)
-        torch.cuda.synchronize()
-        idc = ids.cpu()
-        u = [len(set(idc[l].flatten().tolist())) for l in range(NL)]
-        uniq.extend(u)
-        bytes_per_input.append(sum(ROUTER_BYTES + (n + 1) * expert_bytes for n in u))
-    # Prime one cached graph per input buffer (the graph bakes in pointers).
-    for i, x in enumerate(xs):
-        F.decode_stack(layers, x, ys[i], ws)
-    torch.cuda.synchronize()
-    assert F.device_error() == 0
+    extras = {}
+    if wl.get("prefill"):
+        res = measure_prefill(F, synth, torch, name, args.steps, args.warmup, world, dev, local)
+    else:
+        layers = build_stack(F, synth, torch, wl["fmt"], dev, args.layers)
+        res = measure_stack(F, synth, torch, name, layers, args.steps, args.warmup, world, dev, local)
+        if name == "stack47_b1_nvfp4" and not args.no_extras:
+            # batch 8 on the same resident weights
+            extras["batch8"] = dict(workload="stack47_b8_nvfp4", **measure_stack(
+                F, synth, torch, "stack47_b8_nvfp4", layers, max(10, args.steps // 4), args.warmup, world, dev,
+                local))
+        del layers
+        F.release()
+        torch.cuda.empty_cache()
+        if name == "stack47_b1_nvfp4" and not args.no_extras:
+            extras["prefill"] = dict(workload="prefill8192_nvfp4", **measure_prefill(
+                F, synth, torch, "prefill8192_nvfp4", max(5, args.steps // 40), 3, world, dev, local))
+            torch.cuda.empty_cache()
+            layers = build_stack(F, synth, torch, "bf16", dev, args.layers)
+            extras["bf16_batch8"] = dict(workload="stack47_b8_bf16", **measure_stack(
+                F, synth, torch, "stack47_b8_bf16", layers, max(10, args.steps // 8), args.warmup, world, dev,
+                local))
+            del layers
+            F.release()
+            torch.cuda.empty_cache()
 
-    stream = torch.cuda.current_stream()
-    for s in range(args.warmup):
-        F.decode_stack(layers, xs[s % N_INPUTS], ys[s % N_INPUTS], ws)
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        tdist.barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for s in range(args.steps):
-        F.decode_stack(layers, xs[s % N_INPUTS], ys[s % N_INPUTS], ws)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tdist.barrier()
-    clk = clocks.stop()
-    err = F.device_error()
-
-    # End to end through the C ABI: pinned host input -> device, stack, device -> pinned host.
-    hx = [x.cpu().pin_memory() for x in xs]
-    hy = torch.empty_like(hx[0]).pin_memory()
-    xin = torch.empty_like(xs[0])
-    yout = torch.empty_like(xs[0])
-    for s in range(max(3, args.warmup)):
-        xin.copy_(hx[s % N_INPUTS], non_blocking=True)
-        F.decode_stack(layers, xin, yout, ws)
-        hy.copy_(yout, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_steps = max(10, args.steps // 2)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(e2e_steps):
-        xin.copy_(hx[s % N_INPUTS], non_blocking=True)
-        F.decode_stack(layers, xin, yout, ws)
-        hy.copy_(yout, non_blocking=True)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = t0.elapsed_time(t1) / e2e_steps
-
-    ms_t = torch.tensor([ms], device=dev)
-    if world > 1:
-        tdist.all_reduce(ms_t, op=tdist.ReduceOp.MAX)
-    ms = float(ms_t.item())
-    ms_per_step = ms / args.steps
-    us_per_layer = ms_per_step * 1000.0 / NL
-    total_bytes = sum(bytes_per_input[s % N_INPUTS] for s in range(args.steps))
-    gbs = total_bytes / (ms / 1000.0) / 1e9
-    peaks = {}
-    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk_path):
-        peaks = json.load(open(pk_path))
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
-    bytes_per_layer = total_bytes / args.steps / NL
-    traffic_ratio, traffic_src = profiled_traffic_ratio(args.workload)
     out = {
         "metric": METRIC,
-        "value": round(us_per_layer, 3),
+        "value": res["value"],
         "unit": "us/layer",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4),
+        "ms_per_step": res["ms_per_step"],
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "nvfp4-w/bf16-a (f32 accumulate)" if fmt == F.W_NVFP4 else "bf16 (f32 accumulate)",
+        "dtype": dtype_of(wl["fmt"]),
         "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
-        "config": {
-            "workload": args.workload, "layers": NL, "batch": B, "hidden": 2048, "experts": "256+1",
-            "inter": 512, "top_k": 6, "weights": wl["fmt"], "parallelism": f"replicas x{world}",
-            "l2": "inputs larger than L2: 16 rotating batches, >=631 MB touched per step, weights resident "
-                  f"{len(layers) * F.packed_bytes(fmt) / 1e9:.1f} GB",
-            "mean_unique_experts_per_layer": round(sum(uniq) / len(uniq), 2),
-        },
-        "effective_hbm_gbs": round(gbs, 1),
-        "roofline": {
-            "kernel": "decode sublayer (router + gate/up + down, chained by programmatic dependent launch)",
-            "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(gbs / peak, 4), "peak_source": peak_src,
-            "bytes_per_layer": round(bytes_per_layer),
-            "traffic": round(traffic_ratio * bytes_per_layer) if traffic_ratio else None,
-            "traffic_source": traffic_src,
-        },
-        "e2e": {"value": round(e2e_ms * 1000.0 / NL, 3), "unit": "us/layer",
-                "h2d_bytes_per_step": B * 2048 * 2, "d2h_bytes_per_step": B * 2048 * 2},
-        "gpu_launches": args.steps * NL * 3,
-        "clocks": clk,
-        "device_error_word": err,
+        "config": workload_config(name, world, args.layers),
     }
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
+    out.update({k: v for k, v in res.items() if k not in ("value", "unit", "ms_per_step")})
+    if want_cpu:
         try:
-            out["cpu_baseline"] = time_oracle(wl["cfg"], B, wl["fmt"], args.cpu_seconds)
+            if wl.get("prefill"):
+                out["cpu_baseline"] = time_oracle_prefill(wl["cfg"], wl["batch"])
+            else:
+                out["cpu_baseline"] = time_oracle_all(wl["cfg"], wl["batch"], wl["fmt"], args.cpu_seconds)
         except Exception as e:  # report, do not hide
             out["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+        for key, ex in extras.items():
+            try:
+                w2 = WORKLOADS[ex["workload"]]
+                if w2.get("prefill"):
+                    ex["cpu_baseline"] = time_oracle_prefill(w2["cfg"], w2["batch"])
+                else:
+                    ex["cpu_baseline"] = time_oracle(w2["cfg"], w2["batch"], w2["fmt"], args.cpu_seconds / 3)
+            except Exception as e:
+                ex["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
     elif rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = {"value": None, "note": "timed at N=1 only"}
+    out.update(extras)
     if rank == 0:
         print(json.dumps(out), flush=True)
-    F.release()
     if world > 1:
         tdist.destroy_process_group()
 
@@ -570,40 +607,37 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
+    name = args.workload
+    wl = WORKLOADS[name]
+    common = {
+        "impl": "reference", "metric": METRIC, "unit": "us/layer", "n_gpus": world, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
+        "config": workload_config(name, world, args.layers),
+    }
     if wl.get("prefill"):
         r = time_oracle_prefill(wl["cfg"], wl["batch"])
         us = r["value"]
-        print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer", "n_gpus": world,
-            "steps": 1, "warmup": 0, "ms_per_step": round(us / 1000.0, 3), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded generator)",
-            "config": {"workload": args.workload, "tokens": wl["batch"], "weights": wl["fmt"]},
-            "cpu_baseline": r,
-            "e2e": {"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        }), flush=True)
+        print(json.dumps(dict(common, value=round(us, 1), steps=1, warmup=0, ms_per_step=round(us / 1000.0, 3),
+                              cpu_baseline=r,
+                              e2e={"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0,
+                                   "d2h_bytes_per_step": 0})), flush=True)
         return
     per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         time_oracle(wl["cfg"], wl["batch"], wl["fmt"], per_step_budget / 4)
-    vals = []
-    samples = []
+    vals, samples = [], []
     for _ in range(args.steps):
         r = time_oracle(wl["cfg"], wl["batch"], wl["fmt"], per_step_budget)
         vals.append(r["value"])
         samples.append(r["sample"])
     us = statistics.mean(vals)
-    out = {
-        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * N_LAYERS / 1000.0, 3),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-        "data": "synthetic (seeded generator)",
-        "config": {"workload": args.workload, "layers": N_LAYERS, "batch": wl["batch"], "weights": wl["fmt"]},
-        "cpu_baseline": {"value": round(us, 1), "unit": "us/layer", "cores": 1, "kind": "oracle",
-                         "sample": samples[-1] if samples else ""},
-        "e2e": {"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(out), flush=True)
+    print(json.dumps(dict(common, value=round(us, 1), steps=args.steps, warmup=args.warmup,
+                          ms_per_step=round(us * args.layers / 1000.0, 3),
+                          cpu_baseline={"value": round(us, 1), "unit": "us/layer", "cores": 1, "kind": "oracle",
+                                        "sample": samples[-1] if samples else ""},
+                          e2e={"value": round(us, 1), "unit": "us/layer", "h2d_bytes_per_step": 0,
+                               "d2h_bytes_per_step": 0})), flush=True)
 
 
 def main():

@@ -16,7 +16,10 @@
  *   - All tensor pointers are DEVICE pointers (the current CUDA device) owned
  *     by the caller; every pointer must be 16-byte aligned.  Row-major layouts.
  *   - Arguments are validated on the host before anything is enqueued; an
- *     invalid call returns a negative status and enqueues nothing.
+ *     invalid call returns a negative status and enqueues nothing.  A buffer
+ *     the call writes (outputs, workspace) must not share a byte with any
+ *     other buffer of the call, weights included (FLINT_MOE_ERR_INVALID_ARG);
+ *     buffers that are only read may overlap.
  *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
  *     stream); outputs are valid after the stream is synchronised.
  *   - The library allocates no device memory on the compute path: scratch
@@ -113,14 +116,17 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
 /*
  * One MoE sublayer for a decode batch of 1..8 independent tokens.
  *   x        bf16 [B][H] input (RMSNorm'd first if layer->norm_w != NULL)
- *   y        bf16 [B][H] output; must not overlap x (nor either of them the
- *            workspace: FLINT_MOE_ERR_INVALID_ARG)
+ *   y        bf16 [B][H] output
  *   topk_ids int32 [B][6] selected experts (descending score) or NULL
  *   topk_w   fp32  [B][6] their renormalised weights, or NULL
- * Three kernels chained with programmatic dependent launch: the router GEMV
- * with sigmoid top-6; the gate/up GEMV with SiLU*up over the selected experts
- * only; the down GEMV fused with the weighted combine and the shared expert.
- * B > 8 returns FLINT_MOE_ERR_UNSUPPORTED.
+ * NVFP4 weights: one cooperative kernel, one thread block per SM (at least
+ * 128 SMs, else FLINT_MOE_ERR_UNSUPPORTED), that runs the router GEMV with
+ * sigmoid top-6, the gate/up GEMV with SiLU*up over the selected experts only,
+ * and the down GEMV fused with the weighted combine and the shared expert; its
+ * blocks exchange logits, h and y through the workspace.  BF16 weights: the
+ * same three steps as three kernels chained with programmatic dependent
+ * launch.  B > 8 returns FLINT_MOE_ERR_UNSUPPORTED.  The result is
+ * deterministic: the same inputs give the same bits on every call.
  */
 int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
                            const void *x, int B, void *y, int32_t *topk_ids,
@@ -130,15 +136,19 @@ int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *la
 /*
  * n_layers chained sublayers for one decode batch: sublayer i+1 reads
  * sublayer i's output (through its own RMSNorm when layers[i+1].norm_w is
- * set; no residual is added).  The chain of 3*n_layers kernels is captured
- * once into a CUDA graph (cached per argument set; see flint_moe_release) and
- * replayed with one graph launch per call.
- *   x, y            bf16 [B][H]; must not overlap each other or the workspace
+ * set; no residual is added).
+ *   x, y            bf16 [B][H]
  *   ids_per_layer   int32 [n_layers][B][6] or NULL
  *   w_per_layer     fp32  [n_layers][B][6] or NULL
  *   ys_per_layer    bf16  [n_layers][B][H] every sublayer's output, or NULL
- * The graph bakes in every pointer: a call with the same pointers replays the
- * cached graph, so buffer contents may change between calls, addresses not.
+ * NVFP4 weights: one cooperative kernel launch per 64 sublayers, which
+ * prefetches each sublayer's router rows and shared-expert tiles while the
+ * sublayer before it runs.  BF16 weights: the chain of 3*n_layers kernels is
+ * captured once into a CUDA graph (cached per argument set; see
+ * flint_moe_release) and replayed with one graph launch per call; the graph
+ * bakes in every pointer, so buffer contents may change between calls,
+ * addresses not.  A stack call gives the same bits as the chain of
+ * flint_moe_decode_layer calls over the same sublayers.
  */
 int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *layers,
                            int n_layers, const void *x, int B, void *y,
@@ -172,7 +182,7 @@ int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *l
 
 /* Size of the scratch area built into the library for
  * flint_moe_decode_layer_noalloc, and the largest batch it serves. */
-#define FLINT_MOE_NOALLOC_SCRATCH_BYTES 589824
+#define FLINT_MOE_NOALLOC_SCRATCH_BYTES 1048576
 #define FLINT_MOE_NOALLOC_MAX_TOKENS 8
 
 /*
@@ -190,10 +200,11 @@ int flint_moe_prefill_layer(const flint_moe_dims *dims, const flint_moe_layer *l
  *   B > FLINT_MOE_NOALLOC_MAX_TOKENS returns FLINT_MOE_ERR_WORKSPACE (the
  *   built-in scratch holds at most 8 tokens) and enqueues nothing.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
+ * device current); make that first call before any stream capture (a first
+ * call on a capturing stream returns FLINT_MOE_ERR_INVALID_ARG).  Every
  * call on a device shares the one array and it keeps the previous call's
- * contents; the kernels read no scratch word they have not written in the
- * same call, so nothing needs clearing.  Calls whose work overlaps on the GPU
+ * contents; each call clears what it must find cleared, and its kernels read
+ * no other scratch word before writing it.  Calls whose work overlaps on the GPU
  * (different streams, or other threads) race on the array: order them.
  */
 int flint_moe_decode_layer_noalloc(const flint_moe_dims *dims, const flint_moe_layer *layer,
@@ -209,10 +220,28 @@ int flint_moe_release(void);
  * 8 = the prefill router's tensor-core logit of some expert was further from
  * the exact value than its assumed error bound allows, and that token's
  * routing was recomputed from all 256 exact logits (results stay correct);
- * 16 = a prefill kernel found its shared memory misaligned and did nothing.
+ * 16 = a prefill kernel found its shared memory misaligned and did nothing;
+ * 32 = an NVFP4 decode kernel's wait for data of its other thread blocks ran
+ * out (flint_moe_set_wait_limit) and the call was abandoned.
  * Synchronises the device.  Returns the word (0 = none) or a negative
  * status. */
 int flint_moe_device_error(int reset);
+
+/* The current device's error word as a status: FLINT_MOE_OK (no bit, or only
+ * bit 8), FLINT_MOE_ERR_TIMEOUT (bits 1, 2, 4 or 32: a bounded device wait
+ * gave up and the outputs of the calls since the last reset are undefined),
+ * FLINT_MOE_ERR_CUDA (bit 16, or a CUDA failure).  Synchronises the device;
+ * reset != 0 clears the word. */
+int flint_moe_device_status(int reset);
+
+/* Cycle limit (SM clock) of every later NVFP4 decode call's device-side waits
+ * for data that its other thread blocks write.  A wait that runs out sets bit
+ * 32 of the error word and ends the whole call early, with every thread block
+ * returning and no copy left in flight.  The default, restored by
+ * cycles <= 0, is about one second at the maximum SM clock.  Process-wide;
+ * returns FLINT_MOE_OK.  Waits on the library's own bulk copies keep the
+ * default limit. */
+int flint_moe_set_wait_limit(long long cycles);
 
 /* Static text for a status code. */
 const char *flint_moe_status_string(int status);

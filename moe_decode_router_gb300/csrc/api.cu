@@ -1,5 +1,7 @@
-// C ABI of the Flint MoE library: argument validation, per-device set-up, and
-// the CUDA-graph cache of the decode stack.  See include/flint_moe.h.
+// C ABI of the Flint MoE library: argument validation, per-device set-up, the
+// CUDA-graph cache of the BF16 decode stack, and the built-in scratch of the
+// no-allocation decode call.  See include/flint_moe.h.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -18,8 +20,11 @@ __device__ unsigned int g_flint_error;
 
 namespace {
 
-constexpr int MAX_GU_GRID = 512;
 constexpr size_t MAX_GRAPHS = 32;
+
+// Cycle limit of the persistent decode kernel's waits on data of other thread
+// blocks (flint_moe_set_wait_limit).
+std::atomic<long long> g_wait_limit{WAIT_LIMIT_CYCLES};
 
 struct GraphEntry {
   std::vector<uintptr_t> key;
@@ -29,7 +34,8 @@ struct GraphEntry {
 struct DeviceState {
   bool ready = false;
   int sm_count = 0;
-  int gu_grid = 0;
+  int gu_grid = 0;     // three-kernel path: gate/up CTAs
+  int fused_grid = 0;  // persistent kernel: one CTA per SM, at most one per router expert
   unsigned* err = nullptr;
   cudaStream_t capture_stream = nullptr;
   std::vector<GraphEntry> graphs;
@@ -39,6 +45,25 @@ std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
 
 int to_status(cudaError_t e) { return e == cudaSuccess ? FLINT_MOE_OK : FLINT_MOE_ERR_CUDA; }
+
+// Device address of the error word on the current device (looked up once per
+// device; creates nothing).  Called with g_mu held.
+std::map<int, unsigned*> g_err_words;
+int error_word(unsigned** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  auto it = g_err_words.find(dev);
+  if (it == g_err_words.end()) {
+    unsigned* p = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_flint_error) != cudaSuccess || p == nullptr)
+      return FLINT_MOE_ERR_CUDA;
+    it = g_err_words.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return FLINT_MOE_OK;
+}
+
+int fused_grid_for(int sm_count) { return sm_count < E ? sm_count : E; }
 
 // Called with g_mu held.
 int device_state(DeviceState** out) {
@@ -54,9 +79,11 @@ int device_state(DeviceState** out) {
       return FLINT_MOE_ERR_CUDA;
     if (major != 10) return FLINT_MOE_ERR_UNSUPPORTED;  // built for sm_103a only
     s.gu_grid = s.sm_count < MAX_GU_GRID ? s.sm_count : MAX_GU_GRID;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_flint_error) != cudaSuccess)
-      return FLINT_MOE_ERR_CUDA;
+    s.fused_grid = fused_grid_for(s.sm_count);
+    int st = error_word(&s.err);
+    if (st != FLINT_MOE_OK) return st;
     if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (fused_kernels_init(s.sm_count) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (prefill_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&s.capture_stream, cudaStreamNonBlocking) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
@@ -88,16 +115,38 @@ int check_layer(const flint_moe_dims* d, const flint_moe_layer* L) {
 
 bool opt_aligned(const void* p) { return p == nullptr || aligned(p, 16); }
 
+// A byte range [p, p + n) of one argument; null or empty ranges are skipped.
+struct Range {
+  const void* p;
+  size_t n;
+};
+
 // True if the byte ranges [a, a + na) and [b, b + nb) share a byte.
-bool overlap(const void* a, size_t na, const void* b, size_t nb) {
-  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
-  return pa < pb + nb && pb < pa + na;
+bool overlap(const Range& a, const Range& b) {
+  if (a.p == nullptr || b.p == nullptr || a.n == 0 || b.n == 0) return false;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a.p), pb = reinterpret_cast<uintptr_t>(b.p);
+  return pa < pb + b.n && pb < pa + a.n;
 }
 
-// x and y (bf16 [rows][H]) must not overlap each other or the workspace.
-bool io_overlap(const void* x, const void* y, int rows, const void* ws, size_t ws_need) {
-  const size_t act = (size_t)rows * H * 2;
-  return overlap(x, act, y, act) || (ws != nullptr && (overlap(x, act, ws, ws_need) || overlap(y, act, ws, ws_need)));
+// True if a buffer the call writes shares a byte with another buffer of the
+// call (written or read).  Buffers that are only read may share bytes.
+bool outputs_overlap(const std::vector<Range>& outs, const std::vector<Range>& ins) {
+  for (size_t i = 0; i < outs.size(); ++i) {
+    for (size_t j = i + 1; j < outs.size(); ++j)
+      if (overlap(outs[i], outs[j])) return true;
+    for (const Range& r : ins)
+      if (overlap(outs[i], r)) return true;
+  }
+  return false;
+}
+
+// The read-only buffers of one sublayer.
+void add_layer_ranges(const flint_moe_dims* d, const flint_moe_layer& L, std::vector<Range>& ins) {
+  const bool f4 = d->weight_dtype == FLINT_MOE_W_NVFP4;
+  ins.push_back({L.router_w, (size_t)E * H * 2});
+  ins.push_back({L.experts, (size_t)NE * (f4 ? F4_EXPERT : B16_EXPERT)});
+  if (f4) ins.push_back({L.tensor_scales, (size_t)NE * 2 * 4});
+  ins.push_back({L.norm_w, (size_t)H * 2});
 }
 
 LayerArgs layer_args(const flint_moe_layer& L) {
@@ -109,7 +158,7 @@ LayerArgs layer_args(const flint_moe_layer& L) {
   return a;
 }
 
-size_t decode_ws_needed() { return decode_ws_bytes(MAX_GU_GRID); }
+size_t decode_ws_needed() { return decode_path_ws_bytes(); }
 
 // Largest token count of one prefill call (keeps every pair index and
 // work-item count far inside int32).
@@ -120,39 +169,63 @@ constexpr int PREFILL_MAX_TOKENS = 1 << 20;
 // In host code its name is only a stand-in; kernels get the device address
 // looked up below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FLINT_MOE_NOALLOC_SCRATCH_BYTES];
+static_assert(decode_path_ws_bytes() <= FLINT_MOE_NOALLOC_SCRATCH_BYTES,
+              "the built-in scratch must hold the decode workspace of 8 tokens");
 
 struct NoallocState {
   bool ready = false;
   int gu_grid = 0;
+  int fused_grid = 0;
   unsigned* err = nullptr;
   void* scratch = nullptr;
 };
 std::map<int, NoallocState> g_noalloc;
 
 // Once per device, with that device current; creates nothing and allocates
-// nothing.  Called with g_mu held.
-int noalloc_state(NoallocState** out) {
+// nothing.  Its first call on a device must not happen during a stream
+// capture (symbol look-ups are not capturable): that returns
+// FLINT_MOE_ERR_INVALID_ARG.  Called with g_mu held.
+int noalloc_state(cudaStream_t stream, NoallocState** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   NoallocState& s = g_noalloc[dev];
   if (!s.ready) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return FLINT_MOE_ERR_INVALID_ARG;
     int sms = 0, major = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
     if (major != 10) return FLINT_MOE_ERR_UNSUPPORTED;
-    if (decode_ws_bytes(MAX_GU_GRID) > sizeof(g_noalloc_scratch)) return FLINT_MOE_ERR_WORKSPACE;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return FLINT_MOE_ERR_CUDA;
-    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_flint_error) != cudaSuccess)
-      return FLINT_MOE_ERR_CUDA;
+    int st = error_word(&s.err);
+    if (st != FLINT_MOE_OK) return st;
     if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (fused_kernels_init(sms) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     s.scratch = ptr;
     s.gu_grid = sms < MAX_GU_GRID ? sms : MAX_GU_GRID;
+    s.fused_grid = fused_grid_for(sms);
     s.ready = true;
   }
   *out = &s;
   return FLINT_MOE_OK;
+}
+
+// One decode sublayer on either path (NVFP4: persistent kernel; BF16: three
+// chained kernels) over a workspace of decode_ws_needed() bytes.
+int launch_one_layer(const flint_moe_dims* dims, const flint_moe_layer& layer, const void* x, int B, void* y,
+                     int32_t* ids, float* w, void* ws, int gu_grid, int fused_grid, unsigned* err,
+                     cudaStream_t stream) {
+  const LayerArgs la = layer_args(layer);
+  if (dims->weight_dtype == FLINT_MOE_W_NVFP4) {
+    if (fused_grid < DN_TILES) return FLINT_MOE_ERR_UNSUPPORTED;
+    return to_status(launch_fused_stack(&la, 1, x, B, dims->rms_eps, y, nullptr, ids, w, carve_fused_ws(ws),
+                                        fused_grid, err, g_wait_limit.load(), stream));
+  }
+  return to_status(launch_decode_layer_bf16(la, x, nullptr, B, dims->rms_eps, y, nullptr, nullptr, ids, w,
+                                            carve_decode_ws(ws, MAX_GU_GRID), gu_grid, err, stream, true));
 }
 
 }  // namespace
@@ -207,14 +280,16 @@ int flint_moe_decode_layer(const flint_moe_dims* dims, const flint_moe_layer* la
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
-  if (io_overlap(x, y, B, ws, decode_ws_needed())) return FLINT_MOE_ERR_INVALID_ARG;
+  const size_t act = (size_t)B * H * 2, sel = (size_t)B * TOPK * 4;
+  std::vector<Range> ins{{x, act}};
+  add_layer_ranges(dims, *layer, ins);
+  if (outputs_overlap({{y, act}, {ws, decode_ws_needed()}, {topk_ids, sel}, {topk_w, sel}}, ins))
+    return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
-  const DecodeWs w = carve_decode_ws(ws, MAX_GU_GRID);
-  return to_status(launch_decode_layer(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, layer_args(*layer), x,
-                                       nullptr, B, dims->rms_eps, y, nullptr, nullptr, topk_ids, topk_w, w,
-                                       ds->gu_grid, ds->err, reinterpret_cast<cudaStream_t>(stream), true));
+  return launch_one_layer(dims, *layer, x, B, y, topk_ids, topk_w, ws, ds->gu_grid, ds->fused_grid, ds->err,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* layers, int n_layers, const void* x,
@@ -232,7 +307,29 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
       !opt_aligned(w_per_layer) || !opt_aligned(ys_per_layer))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
-  if (io_overlap(x, y, B, ws, decode_ws_needed())) return FLINT_MOE_ERR_INVALID_ARG;
+  {
+    const size_t act = (size_t)B * H * 2, sel = (size_t)n_layers * B * TOPK * 4;
+    std::vector<Range> ins{{x, act}};
+    for (int i = 0; i < n_layers; ++i) add_layer_ranges(dims, layers[i], ins);
+    if (outputs_overlap({{y, act}, {ws, decode_ws_needed()}, {ids_per_layer, sel}, {w_per_layer, sel},
+                         {ys_per_layer, (size_t)n_layers * act}},
+                        ins))
+      return FLINT_MOE_ERR_INVALID_ARG;
+  }
+
+  if (dims->weight_dtype == FLINT_MOE_W_NVFP4) {
+    // One cooperative launch per 64 sublayers; nothing to capture or cache.
+    std::vector<LayerArgs> la;
+    la.reserve((size_t)n_layers);
+    for (int i = 0; i < n_layers; ++i) la.push_back(layer_args(layers[i]));
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState* ds = nullptr;
+    if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+    if (ds->fused_grid < DN_TILES) return FLINT_MOE_ERR_UNSUPPORTED;
+    return to_status(launch_fused_stack(la.data(), n_layers, x, B, dims->rms_eps, y, ys_per_layer, ids_per_layer,
+                                        w_per_layer, carve_fused_ws(ws), ds->fused_grid, ds->err,
+                                        g_wait_limit.load(), reinterpret_cast<cudaStream_t>(stream)));
+  }
 
   std::vector<uintptr_t> key;
   key.reserve(16 + 4 * (size_t)n_layers);
@@ -262,7 +359,6 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
   for (auto& ge : ds->graphs)
     if (ge.key == key) return to_status(cudaGraphLaunch(ge.exec, user));
 
-  const int fmt = dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1;
   const DecodeWs w = carve_decode_ws(ws, MAX_GU_GRID);
   cudaStream_t cs = ds->capture_stream;
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
@@ -279,8 +375,8 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
     void* ys = ys_per_layer ? static_cast<uint8_t*>(ys_per_layer) + (size_t)i * B * H * 2 : nullptr;
     int32_t* ids = ids_per_layer ? ids_per_layer + (size_t)i * B * TOPK : nullptr;
     float* wl = w_per_layer ? w_per_layer + (size_t)i * B * TOPK : nullptr;
-    le = launch_decode_layer(fmt, layer_args(layers[i]), xin, ss_in, B, dims->rms_eps, yout, ys, ss_out, ids, wl, w,
-                             ds->gu_grid, ds->err, cs, true);
+    le = launch_decode_layer_bf16(layer_args(layers[i]), xin, ss_in, B, dims->rms_eps, yout, ys, ss_out, ids, wl, w,
+                                  ds->gu_grid, ds->err, cs, true);
   }
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
@@ -311,14 +407,16 @@ int flint_moe_decode_layer_noalloc(const flint_moe_dims* dims, const flint_moe_l
   if (x == nullptr || y == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
-  if (io_overlap(x, y, B, nullptr, 0)) return FLINT_MOE_ERR_INVALID_ARG;
+  const size_t act = (size_t)B * H * 2, sel = (size_t)B * TOPK * 4;
+  std::vector<Range> ins{{x, act}};
+  add_layer_ranges(dims, *layer, ins);
+  if (outputs_overlap({{y, act}, {topk_ids, sel}, {topk_w, sel}}, ins)) return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   NoallocState* ns = nullptr;
-  if ((st = noalloc_state(&ns)) != FLINT_MOE_OK) return st;
-  const DecodeWs w = carve_decode_ws(ns->scratch, MAX_GU_GRID);
-  return to_status(launch_decode_layer(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, layer_args(*layer), x,
-                                       nullptr, B, dims->rms_eps, y, nullptr, nullptr, topk_ids, topk_w, w,
-                                       ns->gu_grid, ns->err, reinterpret_cast<cudaStream_t>(stream), true));
+  if ((st = noalloc_state(s, &ns)) != FLINT_MOE_OK) return st;
+  return launch_one_layer(dims, *layer, x, B, y, topk_ids, topk_w, ns->scratch, ns->gu_grid, ns->fused_grid, ns->err,
+                          s);
 }
 
 int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* layer, const void* x, int T, void* y,
@@ -333,7 +431,13 @@ int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* l
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
   if (ws_bytes < prefill_ws_bytes(T)) return FLINT_MOE_ERR_WORKSPACE;
-  if (io_overlap(x, y, T, ws, prefill_ws_bytes(T))) return FLINT_MOE_ERR_INVALID_ARG;
+  {
+    const size_t act = (size_t)T * H * 2, sel = (size_t)T * TOPK * 4;
+    std::vector<Range> ins{{x, act}};
+    add_layer_ranges(dims, *layer, ins);
+    if (outputs_overlap({{y, act}, {ws, prefill_ws_bytes(T)}, {topk_ids, sel}, {topk_w, sel}}, ins))
+      return FLINT_MOE_ERR_INVALID_ARG;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
@@ -361,14 +465,27 @@ int flint_moe_release(void) {
 
 int flint_moe_device_error(int reset) {
   std::lock_guard<std::mutex> lk(g_mu);
-  DeviceState* ds = nullptr;
-  int st = device_state(&ds);
+  unsigned* err = nullptr;
+  int st = error_word(&err);
   if (st != FLINT_MOE_OK) return st;
   unsigned v = 0;
   if (cudaDeviceSynchronize() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  if (cudaMemcpy(&v, ds->err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
-  if (reset && cudaMemset(ds->err, 0, sizeof(unsigned)) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+  if (reset && cudaMemset(err, 0, sizeof(unsigned)) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   return (int)(v & 0x7FFFFFFFu);
+}
+
+int flint_moe_device_status(int reset) {
+  const int v = flint_moe_device_error(reset);
+  if (v < 0) return v;
+  if (v & (int)(ERR_WAIT_FULL | ERR_WAIT_EMPTY | ERR_DRAIN | ERR_POLL)) return FLINT_MOE_ERR_TIMEOUT;
+  if (v & (int)ERR_LAYOUT) return FLINT_MOE_ERR_CUDA;
+  return FLINT_MOE_OK;  // ERR_ROUTER_BOUND alone: the routing was recomputed exactly
+}
+
+int flint_moe_set_wait_limit(long long cycles) {
+  g_wait_limit.store(cycles > 0 ? cycles : WAIT_LIMIT_CYCLES);
+  return FLINT_MOE_OK;
 }
 
 const char* flint_moe_status_string(int status) {

@@ -21,84 +21,10 @@
 //                   the down GEMV of every selected expert for its 16 output
 //                   rows and combines them with the routing weights (shared
 //                   expert weight 1) in a fixed order, rounding once to bf16.
-#include "flint_common.cuh"
+#include "decode_common.cuh"
 #include "flint_internal.h"
 
 namespace flint {
-
-// ------------------------------------------------------------------ helpers
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// 2^e as a float for e in [-126, 127].
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
-
-// Exponent that maps a non-negative max |v| into [2^14, 2^15) (0 for 0/inf/nan).
-__device__ __forceinline__ int f16_range_exp(float m) {
-  if (!(m > 0.f) || !(m < INFINITY)) return 0;
-  int e = ((__float_as_uint(m) >> 23) & 0xFF) - 127;
-  if (e < -126) e = -126;  // subnormal max: scale as the smallest normal
-  int s = 14 - e;
-  if (s > 126) s = 126;
-  if (s < -126) s = -126;
-  return s;
-}
-
-// Reduce-scatter of V compensated sums across a warp (V a power of two <= 32).
-// Lane L returns the total of value L >> (5 - log2 V); the lanes sharing a
-// value hold the same total up to the low-order compensation term.
-template <int V>
-__device__ __forceinline__ CSum cs_reduce_scatter(CSum (&v)[V], int lane) {
-#pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int o = 16 >> st;
-    const int n = V >> st;
-    if (n >= 2) {
-      const int h = n >> 1;
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < h; ++i) {
-        CSum send = up ? v[i] : v[i + h];
-        CSum mine = up ? v[i + h] : v[i];
-        CSum recv;
-        recv.s = __shfl_xor_sync(0xffffffffu, send.s, o);
-        recv.c = __shfl_xor_sync(0xffffffffu, send.c, o);
-        cs_merge(mine, recv);
-        v[i] = mine;
-      }
-    } else {
-      CSum recv;
-      recv.s = __shfl_xor_sync(0xffffffffu, v[0].s, o);
-      recv.c = __shfl_xor_sync(0xffffffffu, v[0].c, o);
-      cs_merge(v[0], recv);
-    }
-  }
-  return v[0];
-}
-
-template <int V>
-struct Log2 {
-  static constexpr int value = V <= 1 ? 0 : 1 + Log2<V / 2>::value;
-};
-template <>
-struct Log2<1> {
-  static constexpr int value = 0;
-};
-template <int V>
-struct Pow2Ceil {
-  static constexpr int value = V <= 1 ? 1 : V <= 2 ? 2 : V <= 4 ? 4 : V <= 8 ? 8 : V <= 16 ? 16 : 32;
-};
-
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
 
 // ------------------------------------------------------------------ router
 
@@ -106,6 +32,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 // (u32 each, two 16-bit values), lane = 4 * token + t.  A consumer warp of
 // slice w loads its 16 blocks' fragments with eight 16-byte loads.
 constexpr int XFRAG_WORDS = 8 * 32 * 16 * 2;
+static_assert(decode_ws_bytes(1) == ws_align256((size_t)BMAX * E * 2) + ws_align256((size_t)BMAX * H * 2) +
+                                        2 * ws_align256((size_t)XFRAG_WORDS * 4) + ws_align256(BMAX * 4) +
+                                        ws_align256((size_t)MAX_SLOTS * BMAX * I * 2) + ws_align256(BMAX * 4) +
+                                        ws_align256((size_t)DN_TILES * BMAX * sizeof(CSum)) +
+                                        ws_align256((size_t)BMAX * H * 2),
+              "workspace size and carve-up must agree");
 
 struct RouterParams {
   const __nv_bfloat16* x;       // [B][H]
@@ -311,96 +243,6 @@ __global__ void __launch_bounds__(256, 2) router_kernel(const RouterParams p) {
       }
     }
   }
-}
-
-// ------------------------------------------------------------------ expert GEMV slices
-
-// 16 weight rows x 256 columns (one packed slice in shared memory) times
-// 256 x 8 activations (B fragments in registers), fp32 accumulate.  Four
-// independent accumulator chains keep the tensor pipe busy.
-__device__ __forceinline__ void nvfp4_slice_mma(const uint8_t* sl, int lane, const uint32_t (&bfr)[16][2],
-                                                float (&acc)[4]) {
-  const int g = lane >> 2;
-  const uint4 s0 = *reinterpret_cast<const uint4*>(sl + F4_CODES + g * 16);
-  const uint4 s1 = *reinterpret_cast<const uint4*>(sl + F4_CODES + 128 + g * 16);
-  const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-  float a4[4][4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a4[c][j] = 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint4 cw = *reinterpret_cast<const uint4*>(sl + c * 512 + lane * 16);
-    const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int kb = 4 * c + j;
-      const uint32_t sc = e4m3x2_to_f16x2(sw[kb >> 1] >> ((kb & 1) * 16));
-      uint32_t a0, a1, a2, a3;
-      e2m1x8_to_f16x2(w4[j], a0, a1, a2, a3);
-      a0 = hmul2_lo(a0, sc);
-      a1 = hmul2_hi(a1, sc);
-      a2 = hmul2_lo(a2, sc);
-      a3 = hmul2_hi(a3, sc);
-      mma_f16(a4[j], a0, a1, a2, a3, bfr[kb][0], bfr[kb][1]);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
-}
-
-__device__ __forceinline__ void bf16_slice_mma(const uint8_t* sl, int lane, const uint32_t (&bfr)[16][2],
-                                               float (&acc)[4]) {
-  float a4[4][4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a4[c][j] = 0.f;
-#pragma unroll
-  for (int kb = 0; kb < 16; ++kb) {
-    const uint4 a = *reinterpret_cast<const uint4*>(sl + kb * 512 + lane * 16);
-    mma_bf16(a4[kb & 3], a.x, a.y, a.z, a.w, bfr[kb][0], bfr[kb][1]);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
-}
-
-template <int FMT>
-struct Fmt;
-template <>
-struct Fmt<0> {
-  static constexpr int SLICE = F4_SLICE;
-  static constexpr int GU_TILE = F4_GU_TILE;
-  static constexpr int DN_TILE = F4_DN_TILE;
-  static constexpr size_t EXPERT = F4_EXPERT;
-  static constexpr size_t GU_BYTES = F4_GU_BYTES;
-  __device__ static void slice(const uint8_t* sl, int lane, const uint32_t (&b)[16][2], float (&acc)[4]) {
-    nvfp4_slice_mma(sl, lane, b, acc);
-  }
-};
-template <>
-struct Fmt<1> {
-  static constexpr int SLICE = B16_SLICE;
-  static constexpr int GU_TILE = B16_GU_TILE;
-  static constexpr int DN_TILE = B16_DN_TILE;
-  static constexpr size_t EXPERT = B16_EXPERT;
-  static constexpr size_t GU_BYTES = B16_GU_BYTES;
-  __device__ static void slice(const uint8_t* sl, int lane, const uint32_t (&b)[16][2], float (&acc)[4]) {
-    bf16_slice_mma(sl, lane, b, acc);
-  }
-};
-
-static_assert(sizeof(Routing) % 4 == 0, "Routing must keep 4-byte alignment");
-static_assert(F4_GU_TILE % 128 == 0 && F4_DN_TILE % 128 == 0 && B16_GU_TILE % 128 == 0 &&
-                  B16_DN_TILE % 128 == 0,
-              "stage buffers must keep 16-byte (bulk copy) alignment");
-static_assert(F4_SLICE % 16 == 0 && B16_SLICE % 16 == 0, "slices are read with 16-byte loads");
-
-// Partial accumulators of one item, one warp: [4 registers][32 lanes] fp32.
-// Register j of lane 4g+t holds row g (j < 2) or g + 8 (j >= 2), token 2t + (j & 1).
-__device__ __forceinline__ int red_off(int row, int tk) {
-  return ((row >> 3) * 2 + (tk & 1)) * 32 + 4 * (row & 7) + (tk >> 1);
 }
 
 // ------------------------------------------------------------------ gate/up
@@ -639,7 +481,6 @@ struct DownParams {
   unsigned* err;
 };
 
-constexpr int HS_STRIDE = 520;  // halves per staged h row: 512 + 8 so rows land 4 banks apart
 constexpr int MAX_HPARTS = 512;
 
 template <int NG>
@@ -899,31 +740,14 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
 
 // ------------------------------------------------------------------ host side
 
-constexpr int F4_GU_STAGES = 5;
 constexpr int B16_GU_STAGES = 3;
 // Down kernel: 4 slot groups, small enough to be resident beside a gate/up
 // CTA so that its down tiles stream in while gate/up still runs.  With 8
 // tokens the staged h rows take 58 KB, so the tile ring shrinks to 8 stages.
 constexpr int DN_GROUPS = 4;
-constexpr int F4_DN_STAGES_S = 12, F4_DN_STAGES_L = 8;  // B <= 4 / B > 4
 constexpr int B16_DN_STAGES = 4;
-constexpr int DN_SMALL_MAX_B = 4;
 
-static size_t align256(size_t v) { return (v + 255) / 256 * 256; }
-
-size_t decode_ws_bytes(int gu_grid) {
-  size_t b = 0;
-  b += align256((size_t)BMAX * E * 2);                  // logits
-  b += align256((size_t)BMAX * H * 2);                  // xh_bf16
-  b += align256((size_t)XFRAG_WORDS * 4);               // xfrag_f16
-  b += align256((size_t)XFRAG_WORDS * 4);               // xfrag_bf16
-  b += align256(BMAX * 4);                              // xh_exp
-  b += align256((size_t)MAX_SLOTS * BMAX * I * 2);      // h
-  b += align256((size_t)gu_grid * BMAX * 4);            // hmax_part
-  b += align256((size_t)DN_TILES * BMAX * sizeof(CSum));  // ss_part
-  b += align256((size_t)BMAX * H * 2);                  // y_mid
-  return b;
-}
+static size_t align256(size_t v) { return ws_align256(v); }
 
 DecodeWs carve_decode_ws(void* ws, int gu_grid) {
   uint8_t* p = static_cast<uint8_t*>(ws);
@@ -1011,14 +835,7 @@ static cudaError_t set_smem(K k, size_t bytes) {
 
 cudaError_t decode_kernels_init(int /*device*/) {
   cudaError_t e;
-  if ((e = set_smem(gateup_kernel<0, F4_GU_STAGES>, gateup_smem_bytes<0, F4_GU_STAGES>())) != cudaSuccess) return e;
   if ((e = set_smem(gateup_kernel<1, B16_GU_STAGES>, gateup_smem_bytes<1, B16_GU_STAGES>())) != cudaSuccess) return e;
-  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>,
-                    down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(DN_SMALL_MAX_B))) != cudaSuccess)
-    return e;
-  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(BMAX))) !=
-      cudaSuccess)
-    return e;
   if ((e = set_smem(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(BMAX))) !=
       cudaSuccess)
     return e;
@@ -1029,7 +846,7 @@ cudaError_t decode_kernels_init(int /*device*/) {
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, const void* ss_in, int B, float eps,
+cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const void* ss_in, int B, float eps,
                                 void* y, void* ys_copy, void* ss_out, int32_t* ids_out, float* w_out,
                                 const DecodeWs& ws, int gu_grid, unsigned* err, cudaStream_t st, bool pdl_first) {
   RouterParams rp;
@@ -1038,7 +855,7 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   rp.norm_w = static_cast<const __nv_bfloat16*>(L.norm_w);
   rp.wr = static_cast<const __nv_bfloat16*>(L.router_w);
   rp.eps = eps;
-  rp.want_f16 = fmt == 0;
+  rp.want_f16 = 0;
   rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
   rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
   rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);
@@ -1051,7 +868,7 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   gp.experts = L.experts;
   gp.tscale = L.tscale;
   gp.logits = rp.logits;
-  gp.xfrag = fmt == 0 ? rp.xfrag_f16 : rp.xfrag_bf16;
+  gp.xfrag = rp.xfrag_bf16;
   gp.xh_exp = ws.xh_exp;
   gp.B = B;
   gp.h = static_cast<__nv_bfloat16*>(ws.h);
@@ -1059,12 +876,8 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   gp.ids_out = ids_out;
   gp.w_out = w_out;
   gp.err = err;
-  if (fmt == 0)
-    e = launch(gateup_kernel<0, F4_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<0, F4_GU_STAGES>(), st, true,
-               gp);
-  else
-    e = launch(gateup_kernel<1, B16_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<1, B16_GU_STAGES>(), st,
-               true, gp);
+  e = launch(gateup_kernel<1, B16_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<1, B16_GU_STAGES>(), st, true,
+             gp);
   if (e != cudaSuccess) return e;
 
   DownParams dp;
@@ -1080,17 +893,8 @@ cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, cons
   dp.ss_out = static_cast<CSum*>(ss_out);
   dp.err = err;
   constexpr int NT = DnCfg<DN_GROUPS>::THREADS;
-  if (fmt == 0) {
-    if (B <= DN_SMALL_MAX_B)
-      e = launch(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>, DN_TILES, NT,
-                 down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(B), st, true, dp);
-    else
-      e = launch(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, DN_TILES, NT,
-                 down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(B), st, true, dp);
-  } else {
-    e = launch(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, DN_TILES, NT, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(B),
-               st, true, dp);
-  }
+  e = launch(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, DN_TILES, NT, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(B),
+             st, true, dp);
   return e;
 }
 

@@ -62,6 +62,10 @@ constexpr unsigned ERR_ROUTER_BOUND = 8u;
 // no work.
 constexpr unsigned ERR_LAYOUT = 16u;
 
+// A wait of the persistent decode kernel for data written by another thread
+// block gave up (its cycle limit ran out); the call was abandoned.
+constexpr unsigned ERR_POLL = 32u;
+
 // A bounded wait gives up after about one second at the maximum SM clock.
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;
 

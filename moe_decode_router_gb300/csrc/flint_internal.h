@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "flint_common.cuh"
+
 namespace flint {
 
 // Workspace carve-up for the decode path (one sublayer in flight at a time;
@@ -22,7 +24,21 @@ struct DecodeWs {
   void* y_mid;       // bf16 [8][2048] output of a non-final stack sublayer
 };
 
-size_t decode_ws_bytes(int gu_grid);
+constexpr size_t ws_align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Largest gate/up grid of the three-kernel path (one CTA per SM).
+constexpr int MAX_GU_GRID = 512;
+
+constexpr size_t decode_ws_bytes(int gu_grid) {
+  return ws_align256((size_t)BMAX * E * 2)                      // logits
+         + ws_align256((size_t)BMAX * H * 2)                    // xh_bf16
+         + 2 * ws_align256((size_t)(8 * 32 * 16 * 2) * 4)       // xfrag_f16, xfrag_bf16
+         + ws_align256(BMAX * 4)                                // xh_exp
+         + ws_align256((size_t)MAX_SLOTS * BMAX * I * 2)        // h
+         + ws_align256((size_t)gu_grid * BMAX * 4)              // hmax_part
+         + ws_align256((size_t)DN_TILES * BMAX * sizeof(CSum))  // ss_part
+         + ws_align256((size_t)BMAX * H * 2);                   // y_mid
+}
 DecodeWs carve_decode_ws(void* ws, int gu_grid);
 
 struct LayerArgs {
@@ -32,16 +48,46 @@ struct LayerArgs {
   const void* norm_w;
 };
 
-// Enqueues the three decode kernels of one sublayer.
+// Enqueues the three decode kernels of one BF16-weight sublayer.
 //   x: input rows; ss_in: sum-of-squares partials of x written by the previous
 //   sublayer's down kernel (nullptr: the router computes them itself).
 //   ss_out: where this sublayer's down kernel writes the partials of y (or nullptr).
-cudaError_t launch_decode_layer(int fmt, const LayerArgs& L, const void* x, const void* ss_in, int B,
+cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const void* ss_in, int B,
                                 float eps, void* y, void* ys_copy, void* ss_out, int32_t* ids_out,
                                 float* w_out, const DecodeWs& ws, int gu_grid, unsigned* err,
                                 cudaStream_t st, bool pdl_first);
 
 cudaError_t decode_kernels_init(int device);
+
+// Persistent NVFP4 decode kernel (decode_fused.cu): one cooperative launch
+// runs up to FUSED_MAX_LAYERS chained sublayers; longer stacks take several.
+constexpr int FUSED_MAX_LAYERS = 64;
+
+// Workspace of the persistent kernel: tagged words (32 data bits + the number
+// of the sublayer that wrote them) through which the CTAs exchange logits, y
+// and h, an abort flag, and the plain output of a stack chunk that feeds the
+// next chunk.
+struct FusedWs {
+  void* logits_t;    // [2][8][256] u64
+  void* y_t;         // [2][8][1024] u64
+  void* h_t;         // [49][8][256] u64
+  unsigned* gabort;  // [1]
+  void* y_mid;       // bf16 [8][2048]
+};
+constexpr size_t fused_ws_bytes() {
+  return ws_align256((size_t)2 * BMAX * E * 8) + ws_align256((size_t)2 * BMAX * (H / 2) * 8) +
+         ws_align256((size_t)MAX_SLOTS * BMAX * (I / 2) * 8) + 256 + ws_align256((size_t)BMAX * H * 2);
+}
+// Decode workspace: either path's layout, whichever is larger.
+constexpr size_t decode_path_ws_bytes() {
+  return decode_ws_bytes(MAX_GU_GRID) > fused_ws_bytes() ? decode_ws_bytes(MAX_GU_GRID) : fused_ws_bytes();
+}
+FusedWs carve_fused_ws(void* ws);
+cudaError_t fused_kernels_init(int sm_count);
+// grid: CTAs of the cooperative launch, one per SM, 128 <= grid <= 256.
+cudaError_t launch_fused_stack(const LayerArgs* layers, int n_layers, const void* x, int B, float eps, void* y,
+                               void* ys, int32_t* ids, float* w, const FusedWs& ws, int grid, unsigned* err,
+                               long long poll_limit, cudaStream_t st);
 
 // Prefill-shaped sublayer over T tokens (NVFP4 weights): workspace size and
 // the enqueue of its kernels on `st`.

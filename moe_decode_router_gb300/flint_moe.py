@@ -76,6 +76,8 @@ _SIGS = {
                                                       ctypes.c_void_p]),
     "flint_moe_release": (ctypes.c_int, []),
     "flint_moe_device_error": (ctypes.c_int, [ctypes.c_int]),
+    "flint_moe_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "flint_moe_set_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
     "flint_moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -302,6 +304,18 @@ def device_error(reset: bool = True) -> int:
     if rc < 0:
         raise FlintMoeError(rc, "flint_moe_device_error")
     return rc
+
+
+def device_status(reset: bool = True) -> int:
+    """The device error word mapped to a status: FLINT_MOE_OK, FLINT_MOE_ERR_TIMEOUT
+    (a bounded device wait gave up) or FLINT_MOE_ERR_CUDA."""
+    return int(_lib().flint_moe_device_status(1 if reset else 0))
+
+
+def set_wait_limit(cycles: int = 0):
+    """Cycle limit of later NVFP4 decode calls' waits on data of their other thread
+    blocks; 0 restores the default (about one second)."""
+    _check(_lib().flint_moe_set_wait_limit(int(cycles)), "flint_moe_set_wait_limit")
 
 
 def alloc_workspace(weight_dtype=W_NVFP4, max_tokens=MAX_DECODE_BATCH, device="cuda"):

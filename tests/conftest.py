@@ -27,3 +27,15 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    # How often the output checks used the one-ulp slack of the tolerance.
+    lib = sys.modules.get("flint_testlib")
+    if lib is None or lib.SLACK_TOTALS["checks"] == 0:
+        return
+    t = lib.SLACK_TOTALS
+    terminalreporter.write_line(
+        f"output checks: {t['checks']}, elements {t['elements']}, beyond 2e-2*rms by at most one bf16 ulp: "
+        f"{t['over_strict']} ({t['over_strict'] / max(1, t['elements']):.2e}); worst single check "
+        f"{t['worst_fraction']:.2e} (limit 1e-2)")

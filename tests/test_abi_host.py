@@ -50,6 +50,12 @@ def test_packed_and_workspace_sizes(lib):
 
 FAKE = 0x7f0000000000  # 256-aligned address never dereferenced: validation fails first
 
+# The calls below pass fake device addresses that must be refused on the host.
+# Where a GPU is visible, a call whose arguments were wrongly valid would launch
+# kernels on them, so these tests run only where no GPU is visible.
+no_gpu_only = pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                                 reason="host-validation tests pass fake device addresses")
+
 
 def _layer(**kw):
     base = dict(router_w=FAKE, experts=FAKE + 256, tensor_scales=FAKE + 512, norm_w=None)
@@ -64,6 +70,7 @@ def _decode(lib, d=None, L=None, x=FAKE + 1024, B=1, y=FAKE + 2048, ws=FAKE + 40
     return lib.flint_moe_decode_layer(ctypes.byref(d), ctypes.byref(L), x, B, y, None, None, ws, ws_bytes, None)
 
 
+@no_gpu_only
 def test_decode_rejects_bad_arguments_on_host(lib):
     assert _decode(lib, B=9) == F.FLINT_MOE_ERR_UNSUPPORTED        # beyond the low-latency cap
     assert _decode(lib, B=0) == F.FLINT_MOE_ERR_INVALID_ARG
@@ -85,6 +92,7 @@ def test_decode_rejects_bad_arguments_on_host(lib):
     assert _decode(lib, x=far + 4096, y=FAKE, ws=far) == F.FLINT_MOE_ERR_INVALID_ARG     # ws overlaps x
 
 
+@no_gpu_only
 def test_stack_and_pack_reject_bad_arguments_on_host(lib):
     d = F.dims()
     arr = (F.Layer * 2)(_layer(), _layer(router_w=None))
@@ -118,6 +126,7 @@ def test_status_strings(lib):
     assert lib.flint_moe_status_string(-99) == b"unknown status"
 
 
+@no_gpu_only
 def test_prefill_rejects_bad_arguments_on_host(lib):
     d = F.dims()
     ws_b = F.workspace_bytes(F.W_NVFP4, 8192)
@@ -140,3 +149,61 @@ def test_prefill_rejects_bad_arguments_on_host(lib):
     far = FAKE + (1 << 36)
     assert call(x=FAKE, y=FAKE + act - 16, ws=far) == F.FLINT_MOE_ERR_INVALID_ARG       # y overlaps x
     assert call(x=FAKE, y=FAKE + act, ws=FAKE + 2 * act - 256) == F.FLINT_MOE_ERR_INVALID_ARG  # ws overlaps y
+
+
+@no_gpu_only
+def test_outputs_must_not_overlap_any_other_buffer(lib):
+    """Every buffer a call writes (y, workspace, ids, weights out, per-layer outputs) is
+    checked against every other buffer of the call, weights included.  The fake
+    buffers below lie 2^32 bytes apart, so the unmodified set would pass the host
+    checks; every call changes exactly one address to create one overlap, and so
+    is refused before anything is launched.  The unmodified set is never called."""
+    G = 1 << 32
+    base = FAKE + (1 << 40)
+    RW, EX, TS, NW, X, Y, WS, IDS, WO, YS = (base + k * G for k in range(10))
+    d = F.dims()
+    ws_b = F.workspace_bytes()
+
+    def layer(**kw):
+        a = dict(router_w=RW, experts=EX, tensor_scales=TS, norm_w=NW)
+        a.update(kw)
+        return F.Layer(a["router_w"], a["experts"], a["tensor_scales"], a["norm_w"])
+
+    def dec(x=X, y=Y, ws=WS, ids=IDS, w=WO, L=None):
+        return lib.flint_moe_decode_layer(ctypes.byref(d), ctypes.byref(L or layer()), x, 2, y, ids, w, ws, ws_b,
+                                          None)
+
+    bad = [
+        dict(ids=Y + 4096),                 # ids inside y (B = 2: 8,192 bytes)
+        dict(w=X + 16),                     # weights out inside x
+        dict(ids=WS + 256),                 # ids inside the workspace
+        dict(w=IDS + 32),                   # ids (48 bytes) and weights out share bytes
+        dict(y=EX + 4096),                  # y inside the packed experts
+        dict(w=TS + 512),                   # weights out on the tensor scales
+        dict(ids=NW + 4064),                # ids overlapping the end of the norm weight (4,096 bytes)
+        dict(ws=RW + (1 << 20) - 256),      # workspace starting in the last bytes of the router weights
+    ]
+    for kw in bad:
+        assert dec(**kw) == F.FLINT_MOE_ERR_INVALID_ARG, kw
+
+    arr = (F.Layer * 2)(layer(), layer(router_w=RW + (1 << 24)))
+
+    def stack(ids=IDS, w=WO, ys=YS, y=Y):
+        return lib.flint_moe_decode_stack(ctypes.byref(d), arr, 2, X, 1, y, ids, w, ys, WS, ws_b, None)
+
+    assert stack(ys=Y + 4096 - 16) == F.FLINT_MOE_ERR_INVALID_ARG   # ys overlaps y
+    assert stack(ys=X - 8192 + 16) == F.FLINT_MOE_ERR_INVALID_ARG   # ys (2 layers x 4,096 bytes) reaches into x
+    assert stack(ids=WS + ws_b - 16) == F.FLINT_MOE_ERR_INVALID_ARG  # ids overlaps the workspace's end
+    assert stack(w=IDS + 32) == F.FLINT_MOE_ERR_INVALID_ARG          # 2 layers x 6 ids = 48 bytes
+    assert stack(y=RW + (1 << 24) + 64) == F.FLINT_MOE_ERR_INVALID_ARG  # y on the second layer's router
+
+    pre_ws = F.workspace_bytes(F.W_NVFP4, 64)
+    rc = lib.flint_moe_prefill_layer(ctypes.byref(d), ctypes.byref(layer()), X, 64, Y, Y + 100 * 1024, None, WS,
+                                     pre_ws, None)
+    assert rc == F.FLINT_MOE_ERR_INVALID_ARG  # ids inside y (64 x 2048 x 2 = 256 KiB)
+
+
+def test_wait_limit_and_status_helpers_exist(lib):
+    assert lib.flint_moe_set_wait_limit(0) == F.FLINT_MOE_OK
+    assert lib.flint_moe_set_wait_limit(123456) == F.FLINT_MOE_OK
+    assert lib.flint_moe_set_wait_limit(-1) == F.FLINT_MOE_OK  # restores the default

@@ -211,6 +211,29 @@ def test_full_47_layer_stack_sampled_layers(dev, B):
     F.release()
 
 
+def test_stack_longer_than_one_launch(dev):
+    """65 sublayers (one persistent launch runs at most 64): the same weights at every
+    depth.  The stack must equal the chain of single-sublayer calls bit for bit, and
+    the sublayers on both sides of the launch boundary are checked teacher-forced."""
+    plains, Ls = _stack_layers(1, 2, dev)
+    lws = [O.layer_from_tensors(p) for p in plains]
+    n = 65
+    layers = [Ls[1]] * n  # a normed sublayer repeated; the first input is raw x through its norm
+    x = synth.gen_x(1, 2, index=70)
+    y, ids, w, ys = run_stack(layers, x, dev)
+    cur = x.to(dev)
+    ws = F.alloc_workspace()
+    for i in range(n):
+        nxt = torch.empty_like(cur)
+        F.decode_layer(layers[i], cur, nxt, ws)
+        cur = nxt
+    torch.cuda.synchronize()
+    assert torch.equal(cur.view(torch.int16), y.view(torch.int16))
+    for i in (62, 63, 64):
+        x_in = bf16_to_f64(ys[i - 1])
+        check_layer(x_in, lws[1], bf16_to_f64(ys[i]), ids[i], w[i])
+
+
 @pytest.fixture(scope="module")
 def layer_bf16(dev):
     plain = synth.gen_layer(3, 1, device="cpu")

@@ -1,8 +1,8 @@
 """The prefill call at its largest accepted size, T = 2^20 tokens (about 33 GB
 of device memory with the workspace), through the C ABI.  Every token must get
 six distinct experts and a finite output row; the routing and output rows of
-sampled tokens (the first, the middle, the last and 29 random ones) are checked
-against the oracle."""
+8,192 contiguous tokens in the middle, the last 256-token tile, the first token
+and 29 random ones are checked against the oracle."""
 
 import numpy as np
 import pytest
@@ -42,7 +42,9 @@ def test_prefill_at_the_token_limit():
     assert (srt[:, 1:] != srt[:, :-1]).all()  # six distinct experts per token
     assert bool(torch.isfinite(y).all())
     rng = np.random.default_rng(11)
-    sample = np.unique(np.concatenate([[0, T_MAX // 2, T_MAX - 1], rng.choice(T_MAX, 29, replace=False)]))
+    block = np.arange(T_MAX // 2 - 4096, T_MAX // 2 + 4096)  # 8,192 contiguous rows (32 shared-expert tiles)
+    last_tile = np.arange(T_MAX - 256, T_MAX)
+    sample = np.unique(np.concatenate([[0, T_MAX - 1], block, last_tile, rng.choice(T_MAX, 29, replace=False)]))
     sel = torch.from_numpy(sample).to(dev)
     st = check_prefill(x[sel].cpu(), lw, y[sel], idc[sample], w[sel].cpu().numpy())
     print(f"T={T_MAX} sampled {len(sample)} rows {st}")
