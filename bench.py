@@ -8,9 +8,8 @@ Workloads (weights drawn on the GPU by the seeded generator, 47 distinct sublaye
   stack47_b8_nvfp4   same weights, batch 8
   stack47_b8_bf16    47 chained BF16-expert sublayers, batch 8 (~76 GB)
   prefill8192_nvfp4  one NVFP4 sublayer over 8,192 tokens (tensor-core grouped GEMMs)
-A step is one pass of the 47-sublayer stack over one batch (NVFP4: one
-launch of the persistent decode kernel; BF16: one CUDA-graph launch of 141
-kernels); inputs cycle through 16 seeded batches so routing, and hence the
+A step is one pass of the 47-sublayer stack over one batch (one CUDA-graph
+launch of 141 chained kernels; with the persistent NVFP4 kernel, one launch); inputs cycle through 16 seeded batches so routing, and hence the
 experts touched, changes every step.  The resident weights (21.4 GB NVFP4 /
 76 GB BF16) and the bytes touched per step (>= 631 MB) are far larger than the
 129 MB L2, so weights stream from HBM.
@@ -22,9 +21,9 @@ roofline fraction against the measured HBM copy bandwidth, the end-to-end
 number through the C ABI with host buffers, SM clocks sampled during the timed
 region, and the CPU oracle timed on a bounded sample (`cpu_baseline`: all host
 cores, one independent oracle process per core; `single_core` inside it).
-The default run also measures batch 8, the prefill sublayer and the BF16
-batch-8 stack and reports each under its own key of the same line
-(`--no-extras` skips them).  `--impl reference` times only the oracle, on the
+The default run also measures batch 8, both batches on the persistent NVFP4
+decode kernel, the prefill sublayer and the BF16 batch-8 stack, and reports
+each under its own key of the same line (`--no-extras` skips them).  `--impl reference` times only the oracle, on the
 same workload and with the same `config`.
 """
 
@@ -349,9 +348,12 @@ def barrier(world: int):
         tdist.barrier()
 
 
-def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, world: int, dev, local: int) -> dict:
-    """One decode-stack workload: device time, algorithmic bytes, roofline, e2e, clocks."""
+def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, world: int, dev, local: int,
+                  persistent: bool = False) -> dict:
+    """One decode-stack workload: device time, algorithmic bytes, roofline, e2e, clocks.
+    persistent: NVFP4 weights on the persistent decode kernel instead of the chained kernels."""
     wl = WORKLOADS[name]
+    F.set_decode_kernel(F.DECODE_PERSISTENT if persistent else F.DECODE_CHAINED)
     B = wl["batch"]
     fmt = F.W_NVFP4 if wl["fmt"] == "nvfp4" else F.W_BF16
     NL = len(layers)
@@ -412,18 +414,21 @@ def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, w
     peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback"
     peak = peak or 6800.0
     bytes_per_layer = total_bytes / steps / NL
-    kind = "fused" if fmt == F.W_NVFP4 else "chain"
+    F.set_decode_kernel(F.DECODE_CHAINED)
+    persistent = persistent and fmt == F.W_NVFP4
+    kind = "fused" if persistent else "chain"
     prof, prof_src = profiled_traffic(kind, name)
     traffic = round(float(prof["ratio"]) * bytes_per_layer * NL) if prof else None
-    launches = math.ceil(NL / FUSED_MAX_LAYERS) if fmt == F.W_NVFP4 else 3 * NL
+    launches = math.ceil(NL / FUSED_MAX_LAYERS) if persistent else 3 * NL
     return {
         "value": round(ms_per_step * 1000.0 / NL, 3),
         "unit": "us/layer",
         "ms_per_step": round(ms_per_step, 4),
         "effective_hbm_gbs": round(gbs, 1),
+        "decode_kernel": "persistent" if persistent else "chained",
         "roofline": {
             "kernel": ("decode_fused_kernel: one persistent launch = the whole 47-sublayer step"
-                       if fmt == F.W_NVFP4 else
+                       if persistent else
                        "decode step (router + gate/up + down per sublayer, PDL-chained, one CUDA graph)"),
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "peak_source": peak_src,
@@ -540,10 +545,16 @@ def run_ours(args):
         layers = build_stack(F, synth, torch, wl["fmt"], dev, args.layers)
         res = measure_stack(F, synth, torch, name, layers, args.steps, args.warmup, world, dev, local)
         if name == "stack47_b1_nvfp4" and not args.no_extras:
-            # batch 8 on the same resident weights
+            # batch 8 on the same resident weights, and both batches on the persistent kernel
             extras["batch8"] = dict(workload="stack47_b8_nvfp4", **measure_stack(
                 F, synth, torch, "stack47_b8_nvfp4", layers, max(10, args.steps // 4), args.warmup, world, dev,
                 local))
+            extras["persistent_b1"] = dict(workload="stack47_b1_nvfp4", **measure_stack(
+                F, synth, torch, "stack47_b1_nvfp4", layers, args.steps, args.warmup, world, dev, local,
+                persistent=True))
+            extras["persistent_b8"] = dict(workload="stack47_b8_nvfp4", **measure_stack(
+                F, synth, torch, "stack47_b8_nvfp4", layers, max(10, args.steps // 4), args.warmup, world, dev,
+                local, persistent=True))
         del layers
         F.release()
         torch.cuda.empty_cache()
@@ -584,6 +595,8 @@ def run_ours(args):
         except Exception as e:  # report, do not hide
             out["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
         for key, ex in extras.items():
+            if key.startswith("persistent"):
+                continue  # same workloads as the lines above; the oracle is timed once per workload
             try:
                 w2 = WORKLOADS[ex["workload"]]
                 if w2.get("prefill"):

@@ -61,6 +61,9 @@ enum { FLINT_MOE_W_NVFP4 = 0, FLINT_MOE_W_BF16 = 1 };
  * low-latency path serves up to 8 requests). */
 #define FLINT_MOE_MAX_DECODE_BATCH 8
 
+/* Decode kernels for NVFP4 weights (flint_moe_set_decode_kernel). */
+enum { FLINT_MOE_DECODE_CHAINED = 0, FLINT_MOE_DECODE_PERSISTENT = 1 };
+
 /* Model dimensions.  Must equal {2048, 256, 1, 512, 6, *, eps}. */
 typedef struct {
     int hidden;       /* H = 2048                                   */
@@ -119,14 +122,16 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
  *   y        bf16 [B][H] output
  *   topk_ids int32 [B][6] selected experts (descending score) or NULL
  *   topk_w   fp32  [B][6] their renormalised weights, or NULL
- * NVFP4 weights: one cooperative kernel, one thread block per SM (at least
- * 128 SMs, else FLINT_MOE_ERR_UNSUPPORTED), that runs the router GEMV with
- * sigmoid top-6, the gate/up GEMV with SiLU*up over the selected experts only,
- * and the down GEMV fused with the weighted combine and the shared expert; its
- * blocks exchange logits, h and y through the workspace.  BF16 weights: the
- * same three steps as three kernels chained with programmatic dependent
- * launch.  B > 8 returns FLINT_MOE_ERR_UNSUPPORTED.  The result is
- * deterministic: the same inputs give the same bits on every call.
+ * Three steps: the router GEMV with sigmoid top-6; the gate/up GEMV with
+ * SiLU*up over the selected experts only; the down GEMV fused with the
+ * weighted combine and the shared expert.  By default (and always for BF16
+ * weights) they are three kernels chained with programmatic dependent launch;
+ * with FLINT_MOE_DECODE_PERSISTENT selected (flint_moe_set_decode_kernel),
+ * NVFP4 weights take one cooperative kernel, one thread block per SM (at
+ * least 128 SMs, else FLINT_MOE_ERR_UNSUPPORTED), whose blocks exchange
+ * logits, h and y through the workspace.  B > 8 returns
+ * FLINT_MOE_ERR_UNSUPPORTED.  The result is deterministic: the same inputs
+ * and kernel choice give the same bits on every call.
  */
 int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
                            const void *x, int B, void *y, int32_t *topk_ids,
@@ -141,14 +146,16 @@ int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *la
  *   ids_per_layer   int32 [n_layers][B][6] or NULL
  *   w_per_layer     fp32  [n_layers][B][6] or NULL
  *   ys_per_layer    bf16  [n_layers][B][H] every sublayer's output, or NULL
- * NVFP4 weights: one cooperative kernel launch per 64 sublayers, which
- * prefetches each sublayer's router rows and shared-expert tiles while the
- * sublayer before it runs.  BF16 weights: the chain of 3*n_layers kernels is
- * captured once into a CUDA graph (cached per argument set; see
+ * Chained kernels (the default, and BF16 weights): the chain of 3*n_layers
+ * kernels is captured once into a CUDA graph (cached per argument set; see
  * flint_moe_release) and replayed with one graph launch per call; the graph
  * bakes in every pointer, so buffer contents may change between calls,
- * addresses not.  A stack call gives the same bits as the chain of
- * flint_moe_decode_layer calls over the same sublayers.
+ * addresses not.  Persistent kernel (NVFP4, flint_moe_set_decode_kernel): one
+ * cooperative launch per 64 sublayers, which prefetches each sublayer's
+ * router rows, norm weight, tensor scales and shared-expert tiles while the
+ * sublayer before it runs.  A stack call gives the same bits as the chain of
+ * flint_moe_decode_layer calls over the same sublayers with the same kernel
+ * choice.
  */
 int flint_moe_decode_stack(const flint_moe_dims *dims, const flint_moe_layer *layers,
                            int n_layers, const void *x, int B, void *y,
@@ -221,8 +228,8 @@ int flint_moe_release(void);
  * the exact value than its assumed error bound allows, and that token's
  * routing was recomputed from all 256 exact logits (results stay correct);
  * 16 = a prefill kernel found its shared memory misaligned and did nothing;
- * 32 = an NVFP4 decode kernel's wait for data of its other thread blocks ran
- * out (flint_moe_set_wait_limit) and the call was abandoned.
+ * 32 = a persistent decode kernel's wait for data of its other thread blocks
+ * ran out (flint_moe_set_wait_limit) and the call was abandoned.
  * Synchronises the device.  Returns the word (0 = none) or a negative
  * status. */
 int flint_moe_device_error(int reset);
@@ -234,7 +241,16 @@ int flint_moe_device_error(int reset);
  * reset != 0 clears the word. */
 int flint_moe_device_status(int reset);
 
-/* Cycle limit (SM clock) of every later NVFP4 decode call's device-side waits
+/* Selects the decode kernels of later NVFP4 calls (decode layer, stack and
+ * the no-allocation call): FLINT_MOE_DECODE_CHAINED (default: router,
+ * gate/up and down kernels chained with programmatic dependent launch) or
+ * FLINT_MOE_DECODE_PERSISTENT (one cooperative kernel per up to 64
+ * sublayers).  Both compute the same sublayer and pass the same parity
+ * tests; BF16 weights always use the chained kernels.  Process-wide; returns
+ * FLINT_MOE_OK or FLINT_MOE_ERR_INVALID_ARG for an unknown value. */
+int flint_moe_set_decode_kernel(int kernel);
+
+/* Cycle limit (SM clock) of every later persistent decode call's device-side waits
  * for data that its other thread blocks write.  A wait that runs out sets bit
  * 32 of the error word and ends the whole call early, with every thread block
  * returning and no copy left in flight.  The default, restored by

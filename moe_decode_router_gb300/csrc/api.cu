@@ -26,6 +26,12 @@ constexpr size_t MAX_GRAPHS = 32;
 // blocks (flint_moe_set_wait_limit).
 std::atomic<long long> g_wait_limit{WAIT_LIMIT_CYCLES};
 
+// Decode kernels used for NVFP4 weights (flint_moe_set_decode_kernel).
+std::atomic<int> g_decode_kernel{FLINT_MOE_DECODE_CHAINED};
+bool use_persistent(const flint_moe_dims* d) {
+  return d->weight_dtype == FLINT_MOE_W_NVFP4 && g_decode_kernel.load() == FLINT_MOE_DECODE_PERSISTENT;
+}
+
 struct GraphEntry {
   std::vector<uintptr_t> key;
   cudaGraphExec_t exec;
@@ -213,19 +219,20 @@ int noalloc_state(cudaStream_t stream, NoallocState** out) {
   return FLINT_MOE_OK;
 }
 
-// One decode sublayer on either path (NVFP4: persistent kernel; BF16: three
-// chained kernels) over a workspace of decode_ws_needed() bytes.
+// One decode sublayer (chained or persistent kernels) over a workspace of
+// decode_ws_needed() bytes.
 int launch_one_layer(const flint_moe_dims* dims, const flint_moe_layer& layer, const void* x, int B, void* y,
                      int32_t* ids, float* w, void* ws, int gu_grid, int fused_grid, unsigned* err,
                      cudaStream_t stream) {
   const LayerArgs la = layer_args(layer);
-  if (dims->weight_dtype == FLINT_MOE_W_NVFP4) {
+  if (use_persistent(dims)) {
     if (fused_grid < DN_TILES) return FLINT_MOE_ERR_UNSUPPORTED;
     return to_status(launch_fused_stack(&la, 1, x, B, dims->rms_eps, y, nullptr, ids, w, carve_fused_ws(ws),
                                         fused_grid, err, g_wait_limit.load(), stream));
   }
-  return to_status(launch_decode_layer_bf16(la, x, nullptr, B, dims->rms_eps, y, nullptr, nullptr, ids, w,
-                                            carve_decode_ws(ws, MAX_GU_GRID), gu_grid, err, stream, true));
+  return to_status(launch_decode_chain(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, la, x, nullptr, B,
+                                       dims->rms_eps, y, nullptr, nullptr, ids, w, carve_decode_ws(ws, MAX_GU_GRID),
+                                       gu_grid, err, stream, true));
 }
 
 }  // namespace
@@ -317,7 +324,7 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
       return FLINT_MOE_ERR_INVALID_ARG;
   }
 
-  if (dims->weight_dtype == FLINT_MOE_W_NVFP4) {
+  if (use_persistent(dims)) {
     // One cooperative launch per 64 sublayers; nothing to capture or cache.
     std::vector<LayerArgs> la;
     la.reserve((size_t)n_layers);
@@ -375,8 +382,8 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
     void* ys = ys_per_layer ? static_cast<uint8_t*>(ys_per_layer) + (size_t)i * B * H * 2 : nullptr;
     int32_t* ids = ids_per_layer ? ids_per_layer + (size_t)i * B * TOPK : nullptr;
     float* wl = w_per_layer ? w_per_layer + (size_t)i * B * TOPK : nullptr;
-    le = launch_decode_layer_bf16(layer_args(layers[i]), xin, ss_in, B, dims->rms_eps, yout, ys, ss_out, ids, wl, w,
-                                  ds->gu_grid, ds->err, cs, true);
+    le = launch_decode_chain(dims->weight_dtype == FLINT_MOE_W_NVFP4 ? 0 : 1, layer_args(layers[i]), xin, ss_in, B,
+                             dims->rms_eps, yout, ys, ss_out, ids, wl, w, ds->gu_grid, ds->err, cs, true);
   }
   cudaGraph_t graph = nullptr;
   e = cudaStreamEndCapture(cs, &graph);
@@ -481,6 +488,12 @@ int flint_moe_device_status(int reset) {
   if (v & (int)(ERR_WAIT_FULL | ERR_WAIT_EMPTY | ERR_DRAIN | ERR_POLL)) return FLINT_MOE_ERR_TIMEOUT;
   if (v & (int)ERR_LAYOUT) return FLINT_MOE_ERR_CUDA;
   return FLINT_MOE_OK;  // ERR_ROUTER_BOUND alone: the routing was recomputed exactly
+}
+
+int flint_moe_set_decode_kernel(int kernel) {
+  if (kernel != FLINT_MOE_DECODE_CHAINED && kernel != FLINT_MOE_DECODE_PERSISTENT) return FLINT_MOE_ERR_INVALID_ARG;
+  g_decode_kernel.store(kernel);
+  return FLINT_MOE_OK;
 }
 
 int flint_moe_set_wait_limit(long long cycles) {

@@ -740,12 +740,15 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
 
 // ------------------------------------------------------------------ host side
 
+constexpr int F4_GU_STAGES = 5;
 constexpr int B16_GU_STAGES = 3;
 // Down kernel: 4 slot groups, small enough to be resident beside a gate/up
 // CTA so that its down tiles stream in while gate/up still runs.  With 8
 // tokens the staged h rows take 58 KB, so the tile ring shrinks to 8 stages.
 constexpr int DN_GROUPS = 4;
+constexpr int F4_DN_STAGES_S = 12, F4_DN_STAGES_L = 8;  // B <= 4 / B > 4
 constexpr int B16_DN_STAGES = 4;
+constexpr int DN_SMALL_MAX_B = 4;
 
 static size_t align256(size_t v) { return ws_align256(v); }
 
@@ -835,7 +838,14 @@ static cudaError_t set_smem(K k, size_t bytes) {
 
 cudaError_t decode_kernels_init(int /*device*/) {
   cudaError_t e;
+  if ((e = set_smem(gateup_kernel<0, F4_GU_STAGES>, gateup_smem_bytes<0, F4_GU_STAGES>())) != cudaSuccess) return e;
   if ((e = set_smem(gateup_kernel<1, B16_GU_STAGES>, gateup_smem_bytes<1, B16_GU_STAGES>())) != cudaSuccess) return e;
+  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>,
+                    down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(DN_SMALL_MAX_B))) != cudaSuccess)
+    return e;
+  if ((e = set_smem(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(BMAX))) !=
+      cudaSuccess)
+    return e;
   if ((e = set_smem(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(BMAX))) !=
       cudaSuccess)
     return e;
@@ -846,7 +856,7 @@ cudaError_t decode_kernels_init(int /*device*/) {
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const void* ss_in, int B, float eps,
+cudaError_t launch_decode_chain(int fmt, const LayerArgs& L, const void* x, const void* ss_in, int B, float eps,
                                 void* y, void* ys_copy, void* ss_out, int32_t* ids_out, float* w_out,
                                 const DecodeWs& ws, int gu_grid, unsigned* err, cudaStream_t st, bool pdl_first) {
   RouterParams rp;
@@ -855,7 +865,7 @@ cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const vo
   rp.norm_w = static_cast<const __nv_bfloat16*>(L.norm_w);
   rp.wr = static_cast<const __nv_bfloat16*>(L.router_w);
   rp.eps = eps;
-  rp.want_f16 = 0;
+  rp.want_f16 = fmt == 0;
   rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
   rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
   rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);
@@ -868,7 +878,7 @@ cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const vo
   gp.experts = L.experts;
   gp.tscale = L.tscale;
   gp.logits = rp.logits;
-  gp.xfrag = rp.xfrag_bf16;
+  gp.xfrag = fmt == 0 ? rp.xfrag_f16 : rp.xfrag_bf16;
   gp.xh_exp = ws.xh_exp;
   gp.B = B;
   gp.h = static_cast<__nv_bfloat16*>(ws.h);
@@ -876,8 +886,12 @@ cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const vo
   gp.ids_out = ids_out;
   gp.w_out = w_out;
   gp.err = err;
-  e = launch(gateup_kernel<1, B16_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<1, B16_GU_STAGES>(), st, true,
-             gp);
+  if (fmt == 0)
+    e = launch(gateup_kernel<0, F4_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<0, F4_GU_STAGES>(), st, true,
+               gp);
+  else
+    e = launch(gateup_kernel<1, B16_GU_STAGES>, gu_grid, GU_THREADS, gateup_smem_bytes<1, B16_GU_STAGES>(), st,
+               true, gp);
   if (e != cudaSuccess) return e;
 
   DownParams dp;
@@ -893,8 +907,17 @@ cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const vo
   dp.ss_out = static_cast<CSum*>(ss_out);
   dp.err = err;
   constexpr int NT = DnCfg<DN_GROUPS>::THREADS;
-  e = launch(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, DN_TILES, NT, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(B),
-             st, true, dp);
+  if (fmt == 0) {
+    if (B <= DN_SMALL_MAX_B)
+      e = launch(down_kernel<0, F4_DN_STAGES_S, DN_GROUPS>, DN_TILES, NT,
+                 down_smem_bytes<0, F4_DN_STAGES_S, DN_GROUPS>(B), st, true, dp);
+    else
+      e = launch(down_kernel<0, F4_DN_STAGES_L, DN_GROUPS>, DN_TILES, NT,
+                 down_smem_bytes<0, F4_DN_STAGES_L, DN_GROUPS>(B), st, true, dp);
+  } else {
+    e = launch(down_kernel<1, B16_DN_STAGES, DN_GROUPS>, DN_TILES, NT, down_smem_bytes<1, B16_DN_STAGES, DN_GROUPS>(B),
+               st, true, dp);
+  }
   return e;
 }
 

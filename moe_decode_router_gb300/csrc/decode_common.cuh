@@ -117,6 +117,60 @@ __device__ __forceinline__ void nvfp4_slice_mma(const uint8_t* sl, int lane, con
   for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
 }
 
+// nvfp4_slice_mma on two slices at once (the same activations), their
+// instruction streams interleaved for latency hiding.  Each slice keeps the
+// four accumulator chains and the final summation order of nvfp4_slice_mma,
+// so its result is bit for bit the same.
+__device__ __forceinline__ void nvfp4_slice_mma2(const uint8_t* sa, const uint8_t* sb, int lane,
+                                                 const uint32_t (&bfr)[16][2], float (&acc_a)[4],
+                                                 float (&acc_b)[4]) {
+  const int g = lane >> 2;
+  uint32_t sw[2][8];
+  {
+    const uint4 a0 = *reinterpret_cast<const uint4*>(sa + F4_CODES + g * 16);
+    const uint4 a1 = *reinterpret_cast<const uint4*>(sa + F4_CODES + 128 + g * 16);
+    const uint4 b0 = *reinterpret_cast<const uint4*>(sb + F4_CODES + g * 16);
+    const uint4 b1 = *reinterpret_cast<const uint4*>(sb + F4_CODES + 128 + g * 16);
+    sw[0][0] = a0.x; sw[0][1] = a0.y; sw[0][2] = a0.z; sw[0][3] = a0.w;
+    sw[0][4] = a1.x; sw[0][5] = a1.y; sw[0][6] = a1.z; sw[0][7] = a1.w;
+    sw[1][0] = b0.x; sw[1][1] = b0.y; sw[1][2] = b0.z; sw[1][3] = b0.w;
+    sw[1][4] = b1.x; sw[1][5] = b1.y; sw[1][6] = b1.z; sw[1][7] = b1.w;
+  }
+  float a4[2][4][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a4[q][c][j] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 ca = *reinterpret_cast<const uint4*>(sa + c * 512 + lane * 16);
+    const uint4 cb = *reinterpret_cast<const uint4*>(sb + c * 512 + lane * 16);
+    const uint32_t w4[2][4] = {{ca.x, ca.y, ca.z, ca.w}, {cb.x, cb.y, cb.z, cb.w}};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kb = 4 * c + j;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t sc = e4m3x2_to_f16x2(sw[q][kb >> 1] >> ((kb & 1) * 16));
+        uint32_t a0, a1, a2, a3;
+        e2m1x8_to_f16x2(w4[q][j], a0, a1, a2, a3);
+        a0 = hmul2_lo(a0, sc);
+        a1 = hmul2_hi(a1, sc);
+        a2 = hmul2_lo(a2, sc);
+        a3 = hmul2_hi(a3, sc);
+        mma_f16(a4[q][j], a0, a1, a2, a3, bfr[kb][0], bfr[kb][1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc_a[j] += (a4[0][0][j] + a4[0][1][j]) + (a4[0][2][j] + a4[0][3][j]);
+    acc_b[j] += (a4[1][0][j] + a4[1][1][j]) + (a4[1][2][j] + a4[1][3][j]);
+  }
+}
+
 __device__ __forceinline__ void bf16_slice_mma(const uint8_t* sl, int lane, const uint32_t (&bfr)[16][2],
                                                float (&acc)[4]) {
   float a4[4][4];

@@ -276,6 +276,7 @@ struct Routing {
   float slot_w[MAX_SLOTS][BMAX];  // routing weight of token t (shared: 1)
   int ids[BMAX][TOPK];
   float w[BMAX][TOPK];
+  uint16_t lg[BMAX][TOPK];        // bf16 bits of the selected logits
   uint32_t umask[8];              // union of the selected experts, 256 bits
   int ubase[8];                   // exclusive prefix of popc(umask)
 };
@@ -298,8 +299,11 @@ __device__ __forceinline__ uint4 load_logits(const __nv_bfloat16* __restrict__ r
 }
 __device__ __forceinline__ float sigmoid_f32(float lg) { return __frcp_rn(__fadd_rn(1.0f, expf(-lg))); }
 
-__device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_out, float* w_out,
-                                          uint32_t* umask) {
+// Selection part of sigmoid top-6: every lane ends with the 6 selected expert
+// indices (descending score, ties to the lower index) and the bf16 bits of
+// their logits.
+__device__ __forceinline__ void warp_top6_core(const uint4 raw, int lane, int (&sel_i)[TOPK],
+                                               uint32_t (&sel_lg)[TOPK]) {
   const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
   uint32_t hb[8], key[8];
 #pragma unroll
@@ -308,18 +312,35 @@ __device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_ou
     const uint32_t ord = (hb[i] & 0x8000u) ? (~hb[i] & 0xFFFFu) : (hb[i] | 0x8000u);
     key[i] = (ord << 16) | (255u - (uint32_t)(lane * 8 + i));
   }
-  // Fast path: top-7 by key (the 7th only to bound the candidates).
-  uint32_t taken = 0u, sel_key[TOPK + 1];
+  // Fast path: top-7 by key (the 7th only to bound the candidates).  Each lane
+  // sorts its 8 keys (descending, a 19-comparator network); the warp maximum of
+  // the lane heads is the next key, and the lane that owned it pops its head.
+  // Keys are distinct (they carry the expert index).
+  {
+#define FLINT_CAS(a, b)                              \
+  {                                                  \
+    const uint32_t hi_ = max(key[a], key[b]);        \
+    key[b] = min(key[a], key[b]);                    \
+    key[a] = hi_;                                    \
+  }
+    FLINT_CAS(0, 2) FLINT_CAS(1, 3) FLINT_CAS(4, 6) FLINT_CAS(5, 7)
+    FLINT_CAS(0, 4) FLINT_CAS(1, 5) FLINT_CAS(2, 6) FLINT_CAS(3, 7)
+    FLINT_CAS(0, 1) FLINT_CAS(2, 3) FLINT_CAS(4, 5) FLINT_CAS(6, 7)
+    FLINT_CAS(2, 4) FLINT_CAS(3, 5)
+    FLINT_CAS(1, 4) FLINT_CAS(3, 6)
+    FLINT_CAS(1, 2) FLINT_CAS(3, 4) FLINT_CAS(5, 6)
+#undef FLINT_CAS
+  }
+  uint32_t sel_key[TOPK + 1];
 #pragma unroll
   for (int k = 0; k < TOPK + 1; ++k) {
-    uint32_t best = 0u;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (!((taken >> i) & 1u) && key[i] > best) best = key[i];
-    const uint32_t m = redux_max(best);
-    const uint32_t idx = 255u - (m & 0xFFu);
-    if ((idx >> 3) == (uint32_t)lane) taken |= 1u << (idx & 7u);
+    const uint32_t m = redux_max(key[0]);
     sel_key[k] = m;
+    if (key[0] == m) {
+#pragma unroll
+      for (int i = 0; i < 7; ++i) key[i] = key[i + 1];
+      key[7] = 0u;
+    }
   }
   bool exact_by_logit = true;
 #pragma unroll
@@ -330,15 +351,12 @@ __device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_ou
     const bool in_band = mag >= 0x3980u && ((bits & 0x8000u) ? mag < 0x42A0u : mag < 0x4100u);
     exact_by_logit = exact_by_logit && in_band;
   }
-  float sel_s[TOPK];
-  int sel_i[TOPK];
   if (exact_by_logit) {
 #pragma unroll
     for (int k = 0; k < TOPK; ++k) {
       const uint32_t ord = sel_key[k] >> 16;
-      const uint32_t bits = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
+      sel_lg[k] = (ord & 0x8000u) ? (ord & 0x7FFFu) : (~ord & 0xFFFFu);
       sel_i[k] = 255 - (int)(sel_key[k] & 0xFFu);
-      sel_s[k] = sigmoid_f32(__uint_as_float(bits << 16));
     }
   } else {
     uint32_t bits[8];
@@ -358,32 +376,72 @@ __device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_ou
       const uint32_t m = redux_max(best);
       const uint32_t win = redux_min(best == m ? bidx : 0xFFFFFFFFu);
       if ((win >> 3) == (uint32_t)lane) tk2 |= 1u << (win & 7u);
-      sel_s[k] = __uint_as_float(m);
+      uint32_t lb = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((int)(win & 7u) == i) lb = hb[i];
+      sel_lg[k] = __shfl_sync(0xffffffffu, lb, (int)(win >> 3));
       sel_i[k] = (int)win;
     }
   }
+}
+
+// Weight part: s = fp32 sigmoid of each selected logit, w_j = s_j / sum of
+// the 6 (fp32, summed in selection order); lanes 0..5 store w_out[lane].
+__device__ __forceinline__ void warp_top6_weights(const uint32_t (&sel_lg)[TOPK], int lane, float* w_out) {
+  float sel_s[TOPK];
+#pragma unroll
+  for (int k = 0; k < TOPK; ++k) sel_s[k] = sigmoid_f32(__uint_as_float(sel_lg[k] << 16));
   float sum = 0.f;
 #pragma unroll
   for (int k = 0; k < TOPK; ++k) sum = __fadd_rn(sum, sel_s[k]);
   if (lane < TOPK) {
     float ws = 0.f;
+#pragma unroll
+    for (int k = 0; k < TOPK; ++k)
+      if (k == lane) ws = sel_s[k];
+    w_out[lane] = __fdiv_rn(ws, sum);
+  }
+}
+
+// Lanes 0..5 store the selection (ids, logit bits) and mark it in umask.
+__device__ __forceinline__ void warp_top6_store(const int (&sel_i)[TOPK], const uint32_t (&sel_lg)[TOPK], int lane,
+                                                int* ids_out, uint16_t* lg_out, uint32_t* umask) {
+  if (lane < TOPK) {
     int wi = 0;
+    uint32_t wl = 0u;
 #pragma unroll
     for (int k = 0; k < TOPK; ++k)
       if (k == lane) {
-        ws = sel_s[k];
         wi = sel_i[k];
+        wl = sel_lg[k];
       }
     ids_out[lane] = wi;
-    w_out[lane] = __fdiv_rn(ws, sum);
+    if (lg_out) lg_out[lane] = (uint16_t)wl;
     atomicOr(&umask[wi >> 5], 1u << (wi & 31));
   }
 }
 
+__device__ __forceinline__ void warp_topk(const uint4 raw, int lane, int* ids_out, float* w_out,
+                                          uint32_t* umask) {
+  int sel_i[TOPK];
+  uint32_t sel_lg[TOPK];
+  warp_top6_core(raw, lane, sel_i, sel_lg);
+  warp_top6_store(sel_i, sel_lg, lane, ids_out, nullptr, umask);
+  warp_top6_weights(sel_lg, lane, w_out);
+}
+
 // Builds the slot table from the per-token selections (one warp).  Slot 0 is
 // the shared expert; slots 1.. are the distinct routed experts in ascending
-// order.  Requires r.umask/ids/w complete and slot_w/slot_mask zeroed.
-__device__ __forceinline__ void warp_slot_table(Routing& r, int B, int lane) {
+// order.  Experts part: n_slots, slot_expert, slot_mask (requires r.umask and
+// r.ids complete and slot_mask zeroed).  Weights part: slot_w (requires r.w
+// and slot_w zeroed).
+__device__ __forceinline__ int slot_of(const Routing& r, int e) {
+  const int wd = e >> 5;
+  return 1 + r.ubase[wd] + __popc(r.umask[wd] & ((1u << (e & 31)) - 1u));
+}
+
+__device__ __forceinline__ void warp_slot_experts(Routing& r, int B, int lane) {
   const uint32_t m = lane < 8 ? r.umask[lane] : 0u;
   const int cnt = __popc(m);
   int incl = cnt;
@@ -410,17 +468,26 @@ __device__ __forceinline__ void warp_slot_table(Routing& r, int B, int lane) {
     r.slot_expert[0] = E;
     r.slot_mask[0] = (1u << B) - 1u;
   }
-  if (lane < B) r.slot_w[0][lane] = 1.0f;
   __syncwarp();
   for (int q = lane; q < B * TOPK; q += 32) {
     const int t = q / TOPK, j = q % TOPK;
-    const int e = r.ids[t][j];
-    const int wd = e >> 5;
-    const int slot = 1 + r.ubase[wd] + __popc(r.umask[wd] & ((1u << (e & 31)) - 1u));
-    r.slot_w[slot][t] = r.w[t][j];
-    atomicOr(&r.slot_mask[slot], 1u << t);
+    atomicOr(&r.slot_mask[slot_of(r, r.ids[t][j])], 1u << t);
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void warp_slot_weights(Routing& r, int B, int lane) {
+  if (lane < B) r.slot_w[0][lane] = 1.0f;
+  for (int q = lane; q < B * TOPK; q += 32) {
+    const int t = q / TOPK, j = q % TOPK;
+    r.slot_w[slot_of(r, r.ids[t][j])][t] = r.w[t][j];
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void warp_slot_table(Routing& r, int B, int lane) {
+  warp_slot_experts(r, B, lane);
+  warp_slot_weights(r, B, lane);
 }
 
 __device__ __forceinline__ void zero_routing(Routing& r, int tid, int nthreads) {

@@ -48,11 +48,11 @@ struct LayerArgs {
   const void* norm_w;
 };
 
-// Enqueues the three decode kernels of one BF16-weight sublayer.
+// Enqueues the three decode kernels of one sublayer (fmt 0 = NVFP4, 1 = BF16).
 //   x: input rows; ss_in: sum-of-squares partials of x written by the previous
 //   sublayer's down kernel (nullptr: the router computes them itself).
 //   ss_out: where this sublayer's down kernel writes the partials of y (or nullptr).
-cudaError_t launch_decode_layer_bf16(const LayerArgs& L, const void* x, const void* ss_in, int B,
+cudaError_t launch_decode_chain(int fmt, const LayerArgs& L, const void* x, const void* ss_in, int B,
                                 float eps, void* y, void* ys_copy, void* ss_out, int32_t* ids_out,
                                 float* w_out, const DecodeWs& ws, int gu_grid, unsigned* err,
                                 cudaStream_t st, bool pdl_first);
@@ -65,18 +65,19 @@ constexpr int FUSED_MAX_LAYERS = 64;
 
 // Workspace of the persistent kernel: tagged words (32 data bits + the number
 // of the sublayer that wrote them) through which the CTAs exchange logits, y
-// and h, an abort flag, and the plain output of a stack chunk that feeds the
-// next chunk.
+// and h, an abort flag, the arrival counters of the three exchanges, and the
+// plain output of a stack chunk that feeds the next chunk.
 struct FusedWs {
   void* logits_t;    // [2][8][256] u64
   void* y_t;         // [2][8][1024] u64
   void* h_t;         // [49][8][256] u64
   unsigned* gabort;  // [1]
+  unsigned* cnt;     // arrival counters, 128 bytes apart: [0] logits, [32] h, [64] y
   void* y_mid;       // bf16 [8][2048]
 };
 constexpr size_t fused_ws_bytes() {
   return ws_align256((size_t)2 * BMAX * E * 8) + ws_align256((size_t)2 * BMAX * (H / 2) * 8) +
-         ws_align256((size_t)MAX_SLOTS * BMAX * (I / 2) * 8) + 256 + ws_align256((size_t)BMAX * H * 2);
+         ws_align256((size_t)MAX_SLOTS * BMAX * (I / 2) * 8) + 512 + ws_align256((size_t)BMAX * H * 2);
 }
 // Decode workspace: either path's layout, whichever is larger.
 constexpr size_t decode_path_ws_bytes() {

@@ -26,6 +26,9 @@ FLINT_MOE_ERR_TIMEOUT = -5
 W_NVFP4 = 0
 W_BF16 = 1
 
+DECODE_CHAINED = 0
+DECODE_PERSISTENT = 1
+
 HIDDEN, N_EXPERTS, N_SHARED, INTER, TOP_K = 2048, 256, 1, 512, 6
 MAX_DECODE_BATCH = 8
 
@@ -78,6 +81,7 @@ _SIGS = {
     "flint_moe_device_error": (ctypes.c_int, [ctypes.c_int]),
     "flint_moe_device_status": (ctypes.c_int, [ctypes.c_int]),
     "flint_moe_set_wait_limit": (ctypes.c_int, [ctypes.c_longlong]),
+    "flint_moe_set_decode_kernel": (ctypes.c_int, [ctypes.c_int]),
     "flint_moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -310,6 +314,11 @@ def device_status(reset: bool = True) -> int:
     """The device error word mapped to a status: FLINT_MOE_OK, FLINT_MOE_ERR_TIMEOUT
     (a bounded device wait gave up) or FLINT_MOE_ERR_CUDA."""
     return int(_lib().flint_moe_device_status(1 if reset else 0))
+
+
+def set_decode_kernel(kernel: int = DECODE_CHAINED):
+    """Decode kernels of later NVFP4 calls: DECODE_CHAINED (default) or DECODE_PERSISTENT."""
+    _check(_lib().flint_moe_set_decode_kernel(int(kernel)), "flint_moe_set_decode_kernel")
 
 
 def set_wait_limit(cycles: int = 0):

@@ -24,6 +24,15 @@ def dev():
     return torch.device("cuda:0")
 
 
+@pytest.fixture(params=[F.DECODE_CHAINED, F.DECODE_PERSISTENT], ids=["chained", "persistent"])
+def kernel(request, dev):
+    """Both NVFP4 decode kernels: the chained router/gate-up/down kernels and the
+    persistent cooperative kernel."""
+    F.set_decode_kernel(request.param)
+    yield request.param
+    F.set_decode_kernel(F.DECODE_CHAINED)
+
+
 def _pack(plain, dev):
     L = F.pack_layer(plain, device=dev)
     torch.cuda.synchronize()
@@ -57,23 +66,23 @@ def run_layer(L, x, dev, ws=None):
 
 
 @pytest.mark.parametrize("B", [1, 2, 3, 5, 8])
-def test_layer_nvfp4_matches_oracle(layer_cfg0, dev, B):
+def test_layer_nvfp4_matches_oracle(layer_cfg0, dev, kernel, B):
     _, lw, L = layer_cfg0
     x = synth.gen_x(0, B, index=10 + B)
     y, ids, w = run_layer(L, x, dev)
     _, st = check_layer(bf16_to_f64(x), lw, bf16_to_f64(y), ids, w)
-    print(f"B={B} {st}")
+    print(f"B={B} kernel={kernel} {st}")
 
 
 @pytest.mark.parametrize("B", [1, 8])
-def test_layer_with_rmsnorm_matches_oracle(layer_norm, dev, B):
+def test_layer_with_rmsnorm_matches_oracle(layer_norm, dev, kernel, B):
     _, lw, L = layer_norm
     x = synth.gen_x(1, B, index=20 + B)
     y, ids, w = run_layer(L, x, dev)
     check_layer(bf16_to_f64(x), lw, bf16_to_f64(y), ids, w)
 
 
-def test_layer_is_deterministic(layer_cfg0, dev):
+def test_layer_is_deterministic(layer_cfg0, dev, kernel):
     _, _, L = layer_cfg0
     x = synth.gen_x(0, 8, index=3)
     y1, i1, w1 = run_layer(L, x, dev)
@@ -82,7 +91,7 @@ def test_layer_is_deterministic(layer_cfg0, dev):
     assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
 
 
-def test_identical_tokens_share_experts(layer_cfg0, dev):
+def test_identical_tokens_share_experts(layer_cfg0, dev, kernel):
     _, lw, L = layer_cfg0
     x = synth.gen_x(0, 1, index=4).repeat(8, 1)
     y, ids, w = run_layer(L, x, dev)
@@ -92,7 +101,7 @@ def test_identical_tokens_share_experts(layer_cfg0, dev):
     check_layer(bf16_to_f64(x), lw, yv, ids, w)
 
 
-def test_unselected_experts_are_never_read(layer_cfg0, dev):
+def test_unselected_experts_are_never_read(layer_cfg0, dev, kernel):
     """Poison every expert no token selects (random codes, NaN block scales): the
     output must stay bit-identical, so the kernels read only selected experts."""
     plain, lw, L = layer_cfg0
@@ -150,7 +159,7 @@ def teacher_forced(x, lws, ids, w, ys, layers_to_check):
 
 
 @pytest.mark.parametrize("B", [1, 4, 8])
-def test_stack_small_teacher_forced(dev, B):
+def test_stack_small_teacher_forced(dev, kernel, B):
     plains, Ls = _stack_layers(1, 3, dev)
     lws = [O.layer_from_tensors(p) for p in plains]
     x = synth.gen_x(1, B, index=30 + B)
@@ -172,7 +181,7 @@ def test_stack_small_teacher_forced(dev, B):
     assert torch.equal(cur.view(torch.int16), y.view(torch.int16))
 
 
-def test_stack_end_to_end_matches_oracle_without_near_ties(dev):
+def test_stack_end_to_end_matches_oracle_without_near_ties(dev, kernel):
     plains, Ls = _stack_layers(1, 3, dev)
     lws = [O.layer_from_tensors(p) for p in plains]
     x = synth.gen_x(1, 4, index=77)
@@ -189,7 +198,7 @@ def test_stack_end_to_end_matches_oracle_without_near_ties(dev):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("B", [1, 8])
-def test_full_47_layer_stack_sampled_layers(dev, B):
+def test_full_47_layer_stack_sampled_layers(dev, kernel, B):
     """The full 47-layer stack at the benchmark's shapes, weights drawn on the GPU;
     sampled sublayers are checked teacher-forced against the oracle."""
     n = synth.N_LAYERS
@@ -211,7 +220,7 @@ def test_full_47_layer_stack_sampled_layers(dev, B):
     F.release()
 
 
-def test_stack_longer_than_one_launch(dev):
+def test_stack_longer_than_one_launch(dev, kernel):
     """65 sublayers (one persistent launch runs at most 64): the same weights at every
     depth.  The stack must equal the chain of single-sublayer calls bit for bit, and
     the sublayers on both sides of the launch boundary are checked teacher-forced."""
@@ -255,3 +264,20 @@ def test_stack_bf16_teacher_forced(dev):
     x = synth.gen_x(3, 8, index=60)
     y, ids, w, ys = run_stack(Ls, x, dev)
     teacher_forced(x, lws, ids, w, ys, range(2))
+
+
+@pytest.mark.parametrize("B", [1, 4, 8])
+def test_chained_and_persistent_kernels_agree(layer_norm, dev, B):
+    """The two NVFP4 decode kernels take the same routing decisions and give outputs
+    within the tolerance of each other on the same sublayer."""
+    _, _, L = layer_norm
+    x = synth.gen_x(1, B, index=80 + B)
+    try:
+        F.set_decode_kernel(F.DECODE_CHAINED)
+        y1, i1, w1 = run_layer(L, x, dev)
+        F.set_decode_kernel(F.DECODE_PERSISTENT)
+        y2, i2, w2 = run_layer(L, x, dev)
+    finally:
+        F.set_decode_kernel(F.DECODE_CHAINED)
+    assert np.array_equal(i1, i2) and np.array_equal(w1, w2)
+    check_output(bf16_to_f64(y2), bf16_to_f64(y1))

@@ -1,6 +1,7 @@
 """Failure detection on the decode path, without a GPU fault: a wait that runs out.
 
-The persistent NVFP4 decode kernel's thread blocks wait for logits, h and y
+The persistent NVFP4 decode kernel's thread blocks (selected with
+flint_moe_set_decode_kernel) wait for logits, h and y
 that the other blocks of the same call write.  Every such wait is bounded
 (flint_moe_set_wait_limit, about one second by default).  With a limit of one
 cycle, a wait that is not satisfied at its first look gives up: it sets bit 32
@@ -33,10 +34,12 @@ def test_wait_that_runs_out_abandons_the_call_and_reports_timeout():
     x = synth.gen_x(1, 8, index=500).to(dev)
     ws = F.alloc_workspace(F.W_NVFP4, 8, device=dev)
     y_ref = torch.empty_like(x)
+    F.set_decode_kernel(F.DECODE_PERSISTENT)
     F.decode_stack(Ls, x, y_ref, ws)
     torch.cuda.synchronize()
     assert F.device_status() == F.FLINT_MOE_OK
 
+    F.set_decode_kernel(F.DECODE_PERSISTENT)
     F.set_wait_limit(1)
     try:
         words = []
@@ -59,6 +62,7 @@ def test_wait_that_runs_out_abandons_the_call_and_reports_timeout():
     y2 = torch.empty_like(x)
     F.decode_stack(Ls, x, y2, ws)
     torch.cuda.synchronize()
+    F.set_decode_kernel(F.DECODE_CHAINED)
     assert F.device_status() == F.FLINT_MOE_OK
     assert torch.equal(y2.view(torch.int16), y_ref.view(torch.int16))
     assert bool(torch.isfinite(y2.float()).all())

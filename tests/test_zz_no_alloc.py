@@ -26,8 +26,10 @@ from moe_decode_router_gb300 import flint_moe as F
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_call_twice_in_a_row():
+@pytest.mark.parametrize("kernel", [F.DECODE_CHAINED, F.DECODE_PERSISTENT], ids=["chained", "persistent"])
+def test_noalloc_matches_workspace_call_twice_in_a_row(kernel):
     lib = F.load_library()
+    F.set_decode_kernel(kernel)
     dev = torch.device("cuda:0")
     plain = synth.gen_layer(0, 0, device="cpu")
     L = F.pack_layer(plain, device=dev)
@@ -60,6 +62,7 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
         # the decode path is deterministic: same kernels, same inputs, same bits
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
         check_output(bf16_to_f64(y), bf16_to_f64(y_ref))
+    F.set_decode_kernel(F.DECODE_CHAINED)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="passes fake device addresses")
