@@ -22,8 +22,9 @@ number through the C ABI with host buffers, SM clocks sampled during the timed
 region, and the CPU oracle timed on a bounded sample (`cpu_baseline`: all host
 cores, one independent oracle process per core; `single_core` inside it).
 The default run also measures batch 8, both batches on the persistent NVFP4
-decode kernel, the prefill sublayer and the BF16 batch-8 stack, and reports
-each under its own key of the same line (`--no-extras` skips them).  `--impl reference` times only the oracle, on the
+decode kernel, the small-batch dense NVFP4 GEMV (8192 x 2048, batch 1 and 8),
+the prefill sublayer and the BF16 batch-8 stack, and reports each under its
+own key of the same line (`--no-extras` skips them).  `--impl reference` times only the oracle, on the
 same workload and with the same `config`.
 """
 
@@ -517,6 +518,70 @@ def measure_prefill(F, synth, torch, name: str, steps: int, warmup: int, world: 
     }
 
 
+DENSE_N, DENSE_K, DENSE_MATS = 8192, 2048, 47
+
+
+def measure_dense(F, synth, torch, B: int, steps: int, warmup: int, world: int, dev, local: int) -> dict:
+    """The small-batch dense GEMV on packed NVFP4: an 8192 x 2048 matrix (the
+    shape of a 4x-wide dense MLP projection of the 2048-wide model), 47 distinct
+    matrices cycled so that the weights stream from HBM (444 MB > L2)."""
+    mats = []
+    for i in range(DENSE_MATS):
+        d = synth.gen_dense(DENSE_N, DENSE_K, index=i, device=dev)
+        mats.append(F.pack_dense(d["codes"], d["scales"], d["tensor_scale"], device=dev))
+        torch.cuda.synchronize()
+        mats[-1]._keepalive = None
+    x = synth.gen_dense_x(B, DENSE_K, index=0, device=dev)
+    y = torch.empty((B, DENSE_N), dtype=torch.bfloat16, device=dev)
+    for s in range(max(3, warmup)):
+        F.dense_gemv(mats[s % DENSE_MATS], x, y)
+    torch.cuda.synchronize()
+    assert F.device_error() == 0
+    # One CUDA graph of 47 calls (one per matrix), as a model's forward would run
+    # them: the time is the GPU's, not the host's launch rate.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(DENSE_MATS):
+            F.dense_gemv(mats[i], x, y)
+    graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    reps = max(3, steps // DENSE_MATS)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    ms = timed(torch, stream, lambda s: graph.replay(), reps)
+    barrier(world)
+    clk = clocks.stop()
+    calls = reps * DENSE_MATS
+    hx = x.cpu().pin_memory()
+    hy = torch.empty((B, DENSE_N), dtype=torch.bfloat16).pin_memory()
+    xin = torch.empty_like(x)
+
+    def e2e_step(s):
+        xin.copy_(hx, non_blocking=True)
+        F.dense_gemv(mats[s % DENSE_MATS], xin, y)
+        hy.copy_(y, non_blocking=True)
+
+    for s in range(3):
+        e2e_step(s)
+    e2e_ms = timed(torch, stream, e2e_step, steps) / steps
+    us = max_over_ranks(torch, ms, world, dev) / calls * 1000.0
+    nbytes = DENSE_N * DENSE_K * 9 // 16
+    gbs = nbytes * world / (us * 1e-6) / 1e9
+    peak = read_peaks().get("hbm_gbs") or 6800.0
+    return {
+        "workload": f"dense_gemv_{DENSE_N}x{DENSE_K}_b{B}_nvfp4", "value": round(us, 3), "unit": "us/call",
+        "effective_hbm_gbs": round(gbs, 1),
+        "roofline": {"kernel": "dense_gemv_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "bytes_per_call": nbytes, "traffic": None},
+        "e2e": {"value": round(e2e_ms * 1000.0, 3), "unit": "us/call", "h2d_bytes_per_step": B * DENSE_K * 2,
+                "d2h_bytes_per_step": B * DENSE_N * 2},
+        "gpu_launches": calls, "timing": "CUDA graph of 47 calls (one per distinct matrix), replayed",
+        "clocks": clk, "device_error_word": F.device_error(),
+    }
+
+
 def dtype_of(fmt: str) -> str:
     return {"nvfp4": "nvfp4-w/bf16-a (f16 operands, f32 accumulate)", "bf16": "bf16 (f32 accumulate)"}[fmt]
 
@@ -559,6 +624,10 @@ def run_ours(args):
         F.release()
         torch.cuda.empty_cache()
         if name == "stack47_b1_nvfp4" and not args.no_extras:
+            for b in (1, 8):
+                extras[f"dense_gemv_b{b}"] = measure_dense(F, synth, torch, b, max(50, args.steps), args.warmup,
+                                                          world, dev, local)
+                torch.cuda.empty_cache()
             extras["prefill"] = dict(workload="prefill8192_nvfp4", **measure_prefill(
                 F, synth, torch, "prefill8192_nvfp4", max(5, args.steps // 40), 3, world, dev, local))
             torch.cuda.empty_cache()
@@ -595,7 +664,7 @@ def run_ours(args):
         except Exception as e:  # report, do not hide
             out["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
         for key, ex in extras.items():
-            if key.startswith("persistent"):
+            if key.startswith("persistent") or key.startswith("dense"):
                 continue  # same workloads as the lines above; the oracle is timed once per workload
             try:
                 w2 = WORKLOADS[ex["workload"]]

@@ -218,6 +218,33 @@ int flint_moe_decode_layer_noalloc(const flint_moe_dims *dims, const flint_moe_l
                                    const void *x, int B, void *y, int32_t *topk_ids,
                                    float *topk_w, flint_moe_stream_t stream);
 
+/*
+ * Small-batch dense GEMV on NVFP4 weights ("Day-0 Support for Flint on vLLM",
+ * section "Optimizations": a small-batch dense GEMV on the same NVFP4 weights
+ * serves the attention projections and the dense MLP of the first layers):
+ *   y[t][n] = bf16( tensor_scale * sum_k x[t][k] * W[n][k] ),  fp32 accumulation,
+ * W[n][k] = e2m1(code) * e4m3(block scale of k / 16).  Shapes: N a multiple
+ * of 16 (below 2^24), K a multiple of 256, at most 32768; otherwise
+ * FLINT_MOE_ERR_UNSUPPORTED.
+ *
+ * flint_moe_dense_packed_bytes: bytes of the packed matrix, N * K * 9 / 16
+ *   (the plain layout's count: the repack is lossless), or 0 for an
+ *   unsupported shape.
+ * flint_moe_pack_dense: one-time repack on `stream` of
+ *   codes  uint8 [N][K/2] (byte j of a row: element 2j low nibble, 2j+1 high)
+ *   scales uint8 [N][K/16] (E4M3 per 16-element block)
+ *   into packed (flint_moe_dense_packed_bytes(N, K) bytes).
+ * flint_moe_dense_gemv: x bf16 [B][K], y bf16 [B][N]; 1 <= B <= 8 and
+ *   B * K <= 32768 (else FLINT_MOE_ERR_UNSUPPORTED).  One kernel on `stream`
+ *   (programmatic dependent launch: it requests its first weight tiles before
+ *   waiting for the kernel before it), deterministic.  No workspace.
+ */
+size_t flint_moe_dense_packed_bytes(int N, int K);
+int flint_moe_pack_dense(const uint8_t *codes, const uint8_t *scales, int N, int K, void *packed,
+                         size_t packed_bytes, flint_moe_stream_t stream);
+int flint_moe_dense_gemv(const void *packed, int N, int K, float tensor_scale, const void *x, int B,
+                         void *y, flint_moe_stream_t stream);
+
 /* Frees cached CUDA graphs of every device the calling thread used.  Call
  * before freeing buffers whose addresses a cached stack graph holds. */
 int flint_moe_release(void);

@@ -90,6 +90,7 @@ int device_state(DeviceState** out) {
     if (st != FLINT_MOE_OK) return st;
     if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (fused_kernels_init(s.sm_count) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (dense_kernels_init() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (prefill_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&s.capture_stream, cudaStreamNonBlocking) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
@@ -450,6 +451,47 @@ int flint_moe_prefill_layer(const flint_moe_dims* dims, const flint_moe_layer* l
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
   return to_status(launch_prefill(layer_args(*layer), x, T, dims->rms_eps, y, topk_ids, topk_w, ws, ds->sm_count,
                                   ds->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Shapes of the dense GEMV: 16 | N, 256 | K, K <= DENSE_MAX_BK, N < 2^24.
+bool dense_shape_ok(int N, int K) {
+  return N >= 16 && N % 16 == 0 && N < (1 << 24) && K >= 256 && K % 256 == 0 && K <= DENSE_MAX_BK;
+}
+
+size_t flint_moe_dense_packed_bytes(int N, int K) { return dense_shape_ok(N, K) ? dense_packed_bytes(N, K) : 0; }
+
+int flint_moe_pack_dense(const uint8_t* codes, const uint8_t* scales, int N, int K, void* packed, size_t packed_bytes,
+                         flint_moe_stream_t stream) {
+  if (!dense_shape_ok(N, K)) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (codes == nullptr || scales == nullptr || packed == nullptr) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(packed, 16)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (packed_bytes < dense_packed_bytes(N, K)) return FLINT_MOE_ERR_WORKSPACE;
+  if (outputs_overlap({{packed, dense_packed_bytes(N, K)}},
+                      {{codes, (size_t)N * K / 2}, {scales, (size_t)N * K / 16}}))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != FLINT_MOE_OK) return st;
+  return to_status(launch_pack_dense(codes, scales, N, K, packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int flint_moe_dense_gemv(const void* packed, int N, int K, float tensor_scale, const void* x, int B, void* y,
+                         flint_moe_stream_t stream) {
+  if (!dense_shape_ok(N, K)) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
+  if (B > BMAX || (long long)B * K > DENSE_MAX_BK) return FLINT_MOE_ERR_UNSUPPORTED;
+  if (packed == nullptr || x == nullptr || y == nullptr) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!aligned(packed, 16) || !aligned(x, 16) || !aligned(y, 16)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(tensor_scale)) return FLINT_MOE_ERR_INVALID_ARG;
+  if (outputs_overlap({{y, (size_t)B * N * 2}}, {{x, (size_t)B * K * 2}, {packed, dense_packed_bytes(N, K)}}))
+    return FLINT_MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState* ds = nullptr;
+  int st = device_state(&ds);
+  if (st != FLINT_MOE_OK) return st;
+  return to_status(launch_dense_gemv(packed, N, K, tensor_scale, x, B, y, ds->sm_count, ds->err,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int flint_moe_release(void) {

@@ -340,7 +340,15 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   // the first routed tiles are in flight.
   uint4 lraw = make_uint4(0u, 0u, 0u, 0u);
   if (warp < B) lraw = load_logits(p.logits + (size_t)warp * E, lane);
-  if (warp < B) warp_topk(lraw, lane, R.ids[warp], R.w[warp], R.umask);
+  if (warp < B) {
+    // The selection alone decides which tiles to read; the routing weights are
+    // only reported (CTA 0), so no other CTA computes them.
+    int sel_i[TOPK];
+    uint32_t sel_lg[TOPK];
+    warp_top6_core(lraw, lane, sel_i, sel_lg);
+    warp_top6_store(sel_i, sel_lg, lane, R.ids[warp], nullptr, R.umask);
+    if (bid == 0 && p.w_out) warp_top6_weights(sel_lg, lane, R.w[warp]);
+  }
   __syncthreads();
   int n_slots = 1;
 #pragma unroll
@@ -355,7 +363,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
     // The slot table is written before any routed tile is requested; a reader
     // of it first waits on such a tile's barrier (or on a partial-sum barrier
     // downstream of one), which orders the table writes before its reads.
-    warp_slot_table(R, B, lane);
+    // This kernel needs the experts and token masks, not the weights.
+    warp_slot_experts(R, B, lane);
     if (lane == 0) {
       for (int n = issued;; ++n) {
         const int i = bid + n * G;

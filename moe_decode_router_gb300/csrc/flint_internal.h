@@ -97,6 +97,16 @@ cudaError_t prefill_kernels_init(int device);
 cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
                            float* w_out, void* ws, int sm_count, unsigned* err, cudaStream_t st);
 
+// Small-batch dense GEMV on packed NVFP4 weights (dense.cu): B * K at most
+// DENSE_MAX_BK (the activations are staged in shared memory).
+constexpr int DENSE_MAX_BK = 32768;
+size_t dense_packed_bytes(int N, int K);
+cudaError_t dense_kernels_init();
+cudaError_t launch_pack_dense(const uint8_t* codes, const uint8_t* scales, int N, int K, void* packed,
+                              cudaStream_t st);
+cudaError_t launch_dense_gemv(const void* packed, int N, int K, float ts, const void* x, int B, void* y, int sm_count,
+                              unsigned* err, cudaStream_t st);
+
 cudaError_t launch_pack(int fmt, const void* gate_up, const uint8_t* gu_scales, const void* down,
                         const uint8_t* dn_scales, void* packed, cudaStream_t st);
 

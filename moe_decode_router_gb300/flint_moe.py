@@ -77,6 +77,11 @@ _SIGS = {
     "flint_moe_decode_layer_noalloc": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(Layer), ctypes.c_void_p,
                                                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                       ctypes.c_void_p]),
+    "flint_moe_dense_packed_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int]),
+    "flint_moe_pack_dense": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "flint_moe_dense_gemv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "flint_moe_release": (ctypes.c_int, []),
     "flint_moe_device_error": (ctypes.c_int, [ctypes.c_int]),
     "flint_moe_device_status": (ctypes.c_int, [ctypes.c_int]),
@@ -297,6 +302,47 @@ def prefill_layer(layer: FlintLayer, x, y, ws, topk_ids=None, topk_w=None, rms_e
                                         _ptr(topk_ids), _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(stream))
     _check(rc, "flint_moe_prefill_layer")
+
+
+class DenseNVFP4:
+    """A packed NVFP4 matrix [N][K] with its fp32 tensor scale, for dense_gemv."""
+
+    def __init__(self, packed, N, K, tensor_scale):
+        self.packed, self.N, self.K, self.tensor_scale = packed, int(N), int(K), float(tensor_scale)
+
+
+def dense_packed_bytes(N: int, K: int) -> int:
+    return int(_lib().flint_moe_dense_packed_bytes(int(N), int(K)))
+
+
+def pack_dense(codes, scales, tensor_scale: float, device="cuda", stream=None) -> DenseNVFP4:
+    """Packs a plain NVFP4 matrix (codes uint8 [N][K/2], scales uint8 [N][K/16])."""
+    if not isinstance(codes, torch.Tensor) or codes.dim() != 2:
+        raise ValueError("codes: expected a 2-D uint8 tensor [N][K/2]")
+    N, K = int(codes.shape[0]), int(codes.shape[1]) * 2
+    codes = codes.to(device).contiguous()
+    scales = scales.to(device).contiguous()
+    _expect(codes, "codes", torch.uint8, (N, K // 2))
+    _expect(scales, "scales", torch.uint8, (N, K // 16))
+    n = dense_packed_bytes(N, K)
+    if n == 0:
+        raise FlintMoeError(FLINT_MOE_ERR_UNSUPPORTED, "flint_moe_dense_packed_bytes")
+    packed = torch.empty(n, dtype=torch.uint8, device=device)
+    rc = _lib().flint_moe_pack_dense(_ptr(codes), _ptr(scales), N, K, _ptr(packed), n, _stream(stream))
+    _check(rc, "flint_moe_pack_dense")
+    w = DenseNVFP4(packed, N, K, tensor_scale)
+    w._keepalive = (codes, scales)  # inputs must live until the pack kernel ran
+    return w
+
+
+def dense_gemv(w: DenseNVFP4, x, y, stream=None):
+    """y[B][N] = bf16(tensor_scale * x[B][K] @ W^T) on the packed NVFP4 matrix."""
+    B = _rows(x)
+    _expect(x, "x", torch.bfloat16, (B, w.K))
+    _expect(y, "y", torch.bfloat16, (B, w.N))
+    _expect(w.packed, "packed", torch.uint8, None)
+    rc = _lib().flint_moe_dense_gemv(_ptr(w.packed), w.N, w.K, w.tensor_scale, _ptr(x), B, _ptr(y), _stream(stream))
+    _check(rc, "flint_moe_dense_gemv")
 
 
 def release():

@@ -45,7 +45,7 @@ __all__ = [
     "bf16_bits_to_f64", "round_f32", "round_bf16", "f64_to_bf16_bits", "round_sum_f32",
     "dequant_nvfp4", "rmsnorm", "router_logits", "sigmoid_scores",
     "topk_desc", "route", "silu_mul", "expert_gate_up", "expert_down",
-    "LayerView", "layer_from_tensors", "moe_layer", "moe_stack", "moe_prefill",
+    "LayerView", "layer_from_tensors", "moe_layer", "moe_stack", "moe_prefill", "dense_gemv",
 ]
 
 H = 2048
@@ -431,3 +431,19 @@ def moe_prefill(x, lw: LayerView, eps=RMS_EPS):
         np.add.at(acc, toks, wt[:, None] * d)
         lw._cache.pop(e, None)
     return dict(y=round_bf16(acc), x_hat=xh, logits=logits, scores=s, ids=ids, weights=w, gap=gap)
+
+
+# ----------------------------------------------------------------------------
+# Small-batch dense GEMV on NVFP4 weights
+# ----------------------------------------------------------------------------
+
+def dense_gemv(x, codes, scales, tensor_scale):
+    """y = bf16( fp32( x . W^T ) ), W = dequant_nvfp4(codes, scales, tensor_scale).
+
+    ("Optimizations": a small-batch dense GEMV on the same NVFP4 weights.)
+    x [B, K] holds bf16 values; codes uint8 [N, K/2] and scales uint8 [N, K/16]
+    in the plain NVFP4 layout.  The dot products are summed in float64 and
+    rounded once to fp32, then to bf16.
+    """
+    w = dequant_nvfp4(codes, scales, tensor_scale)
+    return round_bf16(round_f32(np.atleast_2d(np.asarray(x, np.float64)) @ w.T))

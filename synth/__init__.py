@@ -15,6 +15,8 @@ from .flint_synth import (  # noqa: F401
     TOP_K,
     N_LAYERS,
     config_seed,
+    gen_dense,
+    gen_dense_x,
     gen_layer,
     gen_x,
 )

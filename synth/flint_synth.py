@@ -57,7 +57,13 @@ CONFIGS = {
 _TENSOR_IDS = {
     "x": 1, "router_w": 2, "gu_codes": 3, "gu_scales": 4, "dn_codes": 5,
     "dn_scales": 6, "norm_w": 7, "gu_bf16": 8, "dn_bf16": 9,
+    "dense_codes": 10, "dense_scales": 11, "dense_x": 12,
 }
+
+# Dense NVFP4 matrices (the small-batch dense GEMV): the same element
+# distributions as the expert weights; the seed offset keeps them apart from
+# every workload's layers.
+DENSE_SEED = 0xD3E5
 
 
 def config_seed(cfg: int) -> int:
@@ -131,3 +137,22 @@ def gen_layer(cfg: int, layer: int, device="cpu", weights: str | None = None,
     else:
         out["norm_w"] = None
     return out
+
+
+def gen_dense(N: int, K: int, index: int = 0, device="cpu") -> dict:
+    """A plain NVFP4 matrix [N][K]: codes uint8 [N, K/2] (uniform bytes), E4M3
+    block scales uint8 [N, K/16] (uniform over 0x18..0x48), tensor scale 0.02."""
+    g1 = _gen(DENSE_SEED, index, "dense_codes", device)
+    g2 = _gen(DENSE_SEED, index, "dense_scales", device)
+    return {
+        "codes": torch.randint(0, 256, (N, K // 2), generator=g1, device=device, dtype=torch.uint8),
+        "scales": torch.randint(SCALE_LO, SCALE_HI + 1, (N, K // BLOCK), generator=g2, device=device,
+                                dtype=torch.uint8),
+        "tensor_scale": TENSOR_SCALE,
+    }
+
+
+def gen_dense_x(B: int, K: int, index: int = 0, device="cpu") -> torch.Tensor:
+    """x ~ N(0,1) as bf16 [B, K] for the dense GEMV."""
+    g = _gen(DENSE_SEED, 100000 + index, "dense_x", device)
+    return torch.randn(B, K, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)

@@ -446,3 +446,46 @@ def test_full_size_layer_from_generator():
     assert len(set(r["ids"][0].tolist())) == 6
     rms = np.sqrt(np.mean(r["y"] ** 2))
     assert 1e-3 < rms < 1e4
+
+
+# --------------------------------------------------------------------------- dense GEMV
+
+def test_dense_gemv_exact_on_integer_weights_and_transposition():
+    """Codes in {0, +-1} with scale 1 and tensor scale 1: every product is a small
+    integer, the fp32 sums are exact, and y must equal an int64 matmul (this also
+    catches a transposed operand: N != K below)."""
+    rng = np.random.default_rng(21)
+    N, K = 48, 256
+    vals, codes, scales = _int_nvfp4(rng, N, K)
+    x = rng.integers(-3, 4, size=(5, K))
+    y = O.dense_gemv(x.astype(np.float64), codes, scales, 1.0)
+    assert y.shape == (5, N)
+    ref = x @ vals.T
+    assert np.all(np.abs(ref) < 256)  # exact in bf16
+    assert np.array_equal(y, ref.astype(np.float64))
+
+
+def test_dense_gemv_rounds_once_to_bf16_and_applies_the_tensor_scale():
+    """Hand-worked row: 16 elements of code 0x7 (6.0) with block scale 0x40 (2.0) and
+    tensor scale 0.5 give weights of 6; x = 1 at 16 columns sums to 96 (exact).  A
+    second row of 0x1 (0.5) codes against x = 17 at one column gives 0.5 * 2 * 0.5 *
+    17 = 8.5, and x = 257 at one column of weight 1 gives 257, which rounds to 256 in
+    bf16 (ties to even)."""
+    K = 256
+    codes = np.zeros((3, K // 2), dtype=np.uint8)
+    scales = np.full((3, K // 16), 0x38, dtype=np.uint8)  # 1.0
+    codes[0, :8] = 0x77
+    scales[0, 0] = 0x40
+    codes[1, 0] = 0x01                                      # element 0 = 0.5
+    scales[1, 0] = 0x40
+    codes[2, 0] = 0x02                                      # element 0 = 1.0
+    x = np.zeros((1, K))
+    x[0, :16] = 1.0
+    y = O.dense_gemv(x, codes, scales, 0.5)
+    assert y[0, 0] == 96.0
+    x2 = np.zeros((1, K))
+    x2[0, 0] = 17.0
+    assert O.dense_gemv(x2, codes, scales, 0.5)[0, 1] == 8.5
+    x3 = np.zeros((1, K))
+    x3[0, 0] = 257.0
+    assert O.dense_gemv(x3, codes, scales, 1.0)[0, 2] == 256.0
