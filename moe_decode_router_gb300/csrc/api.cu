@@ -91,6 +91,7 @@ int device_state(DeviceState** out) {
     if (decode_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (fused_kernels_init(s.sm_count) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (dense_kernels_init() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
+    if (medium_kernels_init() != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (prefill_kernels_init(dev) != cudaSuccess) return FLINT_MOE_ERR_CUDA;
     if (cudaStreamCreateWithFlags(&s.capture_stream, cudaStreamNonBlocking) != cudaSuccess)
       return FLINT_MOE_ERR_CUDA;
@@ -252,9 +253,11 @@ size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int max_tokens) {
   if (check_dims(dims) != FLINT_MOE_OK || max_tokens < 1) return 0;
   if (max_tokens > PREFILL_MAX_TOKENS) return 0;
   const size_t dec = decode_ws_needed();
-  if (dims->weight_dtype != FLINT_MOE_W_NVFP4) return max_tokens <= BMAX ? dec : 0;  // prefill: NVFP4 only
-  const size_t pre = prefill_ws_bytes(max_tokens);
-  return pre > dec ? pre : dec;
+  if (dims->weight_dtype != FLINT_MOE_W_NVFP4) return max_tokens <= BMAX ? dec : 0;  // medium, prefill: NVFP4 only
+  size_t n = prefill_ws_bytes(max_tokens);
+  if (n < dec) n = dec;
+  if (max_tokens > BMAX && max_tokens <= MT_MAX && n < medium_ws_bytes()) n = medium_ws_bytes();
+  return n;
 }
 
 int flint_moe_pack_weights(const flint_moe_dims* dims, const void* gate_up, const uint8_t* gate_up_scales,
@@ -283,19 +286,25 @@ int flint_moe_decode_layer(const flint_moe_dims* dims, const flint_moe_layer* la
   if (st != FLINT_MOE_OK) return st;
   if ((st = check_layer(dims, layer)) != FLINT_MOE_OK) return st;
   if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
-  if (B > BMAX) return FLINT_MOE_ERR_UNSUPPORTED;
+  const bool medium = B > BMAX;
+  if (B > MT_MAX || (medium && dims->weight_dtype != FLINT_MOE_W_NVFP4)) return FLINT_MOE_ERR_UNSUPPORTED;
   if (x == nullptr || y == nullptr || ws == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(topk_ids) || !opt_aligned(topk_w))
     return FLINT_MOE_ERR_INVALID_ARG;
-  if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+  const size_t ws_need = medium ? medium_ws_bytes() : decode_ws_needed();
+  if (ws_bytes < ws_need) return FLINT_MOE_ERR_WORKSPACE;
   const size_t act = (size_t)B * H * 2, sel = (size_t)B * TOPK * 4;
   std::vector<Range> ins{{x, act}};
   add_layer_ranges(dims, *layer, ins);
-  if (outputs_overlap({{y, act}, {ws, decode_ws_needed()}, {topk_ids, sel}, {topk_w, sel}}, ins))
+  if (outputs_overlap({{y, act}, {ws, ws_need}, {topk_ids, sel}, {topk_w, sel}}, ins))
     return FLINT_MOE_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
+  if (medium)
+    return to_status(launch_medium_chain(layer_args(*layer), x, B, dims->rms_eps, y, topk_ids, topk_w,
+                                         carve_medium_ws(ws), ds->gu_grid, ds->err,
+                                         reinterpret_cast<cudaStream_t>(stream), true));
   return launch_one_layer(dims, *layer, x, B, y, topk_ids, topk_w, ws, ds->gu_grid, ds->fused_grid, ds->err,
                           reinterpret_cast<cudaStream_t>(stream));
 }
@@ -309,23 +318,25 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
   for (int i = 0; i < n_layers; ++i)
     if ((st = check_layer(dims, &layers[i])) != FLINT_MOE_OK) return st;
   if (B < 1) return FLINT_MOE_ERR_INVALID_ARG;
-  if (B > BMAX) return FLINT_MOE_ERR_UNSUPPORTED;
+  const bool medium = B > BMAX;
+  if (B > MT_MAX || (medium && dims->weight_dtype != FLINT_MOE_W_NVFP4)) return FLINT_MOE_ERR_UNSUPPORTED;
   if (x == nullptr || y == nullptr || ws == nullptr || x == y) return FLINT_MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !opt_aligned(ids_per_layer) ||
       !opt_aligned(w_per_layer) || !opt_aligned(ys_per_layer))
     return FLINT_MOE_ERR_INVALID_ARG;
-  if (ws_bytes < decode_ws_needed()) return FLINT_MOE_ERR_WORKSPACE;
+  const size_t ws_need = medium ? medium_ws_bytes() : decode_ws_needed();
+  if (ws_bytes < ws_need) return FLINT_MOE_ERR_WORKSPACE;
   {
     const size_t act = (size_t)B * H * 2, sel = (size_t)n_layers * B * TOPK * 4;
     std::vector<Range> ins{{x, act}};
     for (int i = 0; i < n_layers; ++i) add_layer_ranges(dims, layers[i], ins);
-    if (outputs_overlap({{y, act}, {ws, decode_ws_needed()}, {ids_per_layer, sel}, {w_per_layer, sel},
+    if (outputs_overlap({{y, act}, {ws, ws_need}, {ids_per_layer, sel}, {w_per_layer, sel},
                          {ys_per_layer, (size_t)n_layers * act}},
                         ins))
       return FLINT_MOE_ERR_INVALID_ARG;
   }
 
-  if (use_persistent(dims)) {
+  if (!medium && use_persistent(dims)) {
     // One cooperative launch per 64 sublayers; nothing to capture or cache.
     std::vector<LayerArgs> la;
     la.reserve((size_t)n_layers);
@@ -368,11 +379,27 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
     if (ge.key == key) return to_status(cudaGraphLaunch(ge.exec, user));
 
   const DecodeWs w = carve_decode_ws(ws, MAX_GU_GRID);
+  const MediumWs mw = carve_medium_ws(ws);
   cudaStream_t cs = ds->capture_stream;
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   cudaError_t le = cudaSuccess;
-  for (int i = 0; i < n_layers && le == cudaSuccess; ++i) {
+  const void* prev = x;
+  for (int i = 0; i < n_layers && le == cudaSuccess && medium; ++i) {
+    // Each sublayer's router computes its own RMSNorm statistics.  A
+    // sublayer's input is read before its output is written, so y_mid can be
+    // both.
+    const bool last = i == n_layers - 1;
+    void* ys = ys_per_layer ? static_cast<uint8_t*>(ys_per_layer) + (size_t)i * B * H * 2 : nullptr;
+    int32_t* ids = ids_per_layer ? ids_per_layer + (size_t)i * B * TOPK : nullptr;
+    float* wl = w_per_layer ? w_per_layer + (size_t)i * B * TOPK : nullptr;
+    void* yout = last ? y : (ys ? ys : mw.y_mid);
+    le = launch_medium_chain(layer_args(layers[i]), prev, B, dims->rms_eps, yout, ids, wl, mw, ds->gu_grid, ds->err,
+                             cs, true);
+    prev = yout;
+    if (le == cudaSuccess && last && ys) le = cudaMemcpyAsync(ys, y, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, cs);
+  }
+  for (int i = 0; i < n_layers && le == cudaSuccess && !medium; ++i) {
     const bool last = i == n_layers - 1;
     const void* xin = i == 0 ? x : w.y_mid;
     void* yout = last ? y : w.y_mid;

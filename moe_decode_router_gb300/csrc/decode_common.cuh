@@ -117,6 +117,47 @@ __device__ __forceinline__ void nvfp4_slice_mma(const uint8_t* sl, int lane, con
   for (int j = 0; j < 4; ++j) acc[j] += (a4[0][j] + a4[1][j]) + (a4[2][j] + a4[3][j]);
 }
 
+// nvfp4_slice_mma against two n8 blocks of activations (16 tokens): every
+// dequantised A fragment feeds two mma, one per block.
+__device__ __forceinline__ void nvfp4_slice_mma_n16(const uint8_t* sl, int lane, const uint32_t (&b0)[16][2],
+                                                    const uint32_t (&b1)[16][2], float (&acc0)[4],
+                                                    float (&acc1)[4]) {
+  const int g = lane >> 2;
+  const uint4 s0 = *reinterpret_cast<const uint4*>(sl + F4_CODES + g * 16);
+  const uint4 s1 = *reinterpret_cast<const uint4*>(sl + F4_CODES + 128 + g * 16);
+  const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  float a4[2][4][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) a4[q][c][j] = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 cw = *reinterpret_cast<const uint4*>(sl + c * 512 + lane * 16);
+    const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kb = 4 * c + j;
+      const uint32_t sc = e4m3x2_to_f16x2(sw[kb >> 1] >> ((kb & 1) * 16));
+      uint32_t a0, a1, a2, a3;
+      e2m1x8_to_f16x2(w4[j], a0, a1, a2, a3);
+      a0 = hmul2_lo(a0, sc);
+      a1 = hmul2_hi(a1, sc);
+      a2 = hmul2_lo(a2, sc);
+      a3 = hmul2_hi(a3, sc);
+      mma_f16(a4[0][j], a0, a1, a2, a3, b0[kb][0], b0[kb][1]);
+      mma_f16(a4[1][j], a0, a1, a2, a3, b1[kb][0], b1[kb][1]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc0[j] += (a4[0][0][j] + a4[0][1][j]) + (a4[0][2][j] + a4[0][3][j]);
+    acc1[j] += (a4[1][0][j] + a4[1][1][j]) + (a4[1][2][j] + a4[1][3][j]);
+  }
+}
+
 // nvfp4_slice_mma on two slices at once (the same activations), their
 // instruction streams interleaved for latency hiding.  Each slice keeps the
 // four accumulator chains and the final summation order of nvfp4_slice_mma,

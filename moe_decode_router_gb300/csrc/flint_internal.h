@@ -97,6 +97,54 @@ cudaError_t prefill_kernels_init(int device);
 cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
                            float* w_out, void* ws, int sm_count, unsigned* err, cudaStream_t st);
 
+// Medium-batch decode path (medium.cu), 9..64 tokens, NVFP4 weights.  Tokens
+// of one expert are processed in slot-chunks of up to MCH tokens (two mma
+// n8 blocks); pairs (token, expert) are numbered expert by expert, the shared
+// expert first.
+constexpr int MT_MAX = 64;
+constexpr int MCH = 16;
+constexpr int MPAIRS = (TOPK + 1) * MT_MAX;
+constexpr int MSC_MAX = 288;  // >= 257 experts + 7 MT_MAX / MCH extra chunks
+static_assert(MSC_MAX >= NE + MPAIRS / MCH, "slot-chunk table");
+struct MedRoute {
+  int n_sc;                        // slot-chunks
+  int n_pairs;                     // 7 T
+  int pad[2];
+  int sc_e[MSC_MAX];               // expert (E = shared)
+  int sc_pair[MSC_MAX];            // pair of its first token
+  int sc_n[MSC_MAX];               // its tokens, 1..MCH
+  uint8_t sc_tok[MSC_MAX][MCH];    // their ids, ascending
+  int pidx[MT_MAX][TOPK + 1];      // pair of (token, j); j = TOPK: the shared expert
+  float w[MT_MAX][TOPK];           // routing weights
+};
+struct MediumWs {
+  void* logits;      // bf16 [64][256]
+  void* xh_bf16;     // bf16 [64][2048]
+  void* xfrag_f16;   // [8 chunks][8 K-slices][32 lanes][32 words]
+  void* xfrag_bf16;  // same layout, bf16 (written by the router, unused here)
+  int* xh_exp;       // [64]
+  MedRoute* rt;
+  void* h;           // bf16 [MPAIRS][512]
+  unsigned* hmax;    // [MPAIRS] fp32 bits of max |h|
+  float* part;       // [MPAIRS][2048] scaled down-projection of each pair
+  void* y_mid;       // bf16 [64][2048] output of a non-final stack sublayer
+};
+constexpr size_t medium_ws_bytes() {
+  return ws_align256((size_t)MT_MAX * E * 2) + ws_align256((size_t)MT_MAX * H * 2) +
+         2 * ws_align256((size_t)(MT_MAX / 8) * 8 * 32 * 32 * 4) + ws_align256(MT_MAX * 4) +
+         ws_align256(sizeof(MedRoute)) + ws_align256((size_t)MPAIRS * I * 2) + ws_align256(MPAIRS * 4) +
+         ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2);
+}
+MediumWs carve_medium_ws(void* ws);
+cudaError_t medium_kernels_init();
+// Router over T <= 64 tokens in chunks of 8 (decode.cu).
+cudaError_t launch_router_chunks(const LayerArgs& L, const void* x, int T, float eps, const MediumWs& ws,
+                                 cudaStream_t st, bool pdl);
+// Enqueues one medium sublayer: router, routing tables, gate/up, down, combine.
+cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
+                                float* w_out, const MediumWs& ws, int sm_count, unsigned* err, cudaStream_t st,
+                                bool pdl_first);
+
 // Small-batch dense GEMV on packed NVFP4 weights (dense.cu): B * K at most
 // DENSE_MAX_BK (the activations are staged in shared memory).
 constexpr int DENSE_MAX_BK = 32768;

@@ -31,6 +31,7 @@ DECODE_PERSISTENT = 1
 
 HIDDEN, N_EXPERTS, N_SHARED, INTER, TOP_K = 2048, 256, 1, 512, 6
 MAX_DECODE_BATCH = 8
+MAX_MEDIUM_BATCH = 64  # decode calls with 9..64 tokens take the medium-batch kernels (NVFP4)
 
 
 class FlintMoeError(RuntimeError):
