@@ -43,6 +43,8 @@ def test_packed_and_workspace_sizes(lib):
     ws = F.workspace_bytes(F.W_NVFP4, 8)
     assert ws > 0 and ws % 256 == 0
     assert F.workspace_bytes(F.W_NVFP4, 1) == ws
+    assert F.workspace_bytes(F.W_NVFP4, 64) > ws                   # medium-batch tables, h and partials
+    assert F.workspace_bytes(F.W_BF16, 9) == 0                     # 9..64 tokens: NVFP4 only
     bad = F.Dims(4096, 256, 1, 512, 6, 0, 1e-6)
     assert lib.flint_moe_packed_bytes(ctypes.byref(bad)) == 0
     assert lib.flint_moe_workspace_bytes(ctypes.byref(bad), 8) == 0
@@ -72,7 +74,9 @@ def _decode(lib, d=None, L=None, x=FAKE + 1024, B=1, y=FAKE + 2048, ws=FAKE + 40
 
 @no_gpu_only
 def test_decode_rejects_bad_arguments_on_host(lib):
-    assert _decode(lib, B=9) == F.FLINT_MOE_ERR_UNSUPPORTED        # beyond the low-latency cap
+    assert _decode(lib, B=65) == F.FLINT_MOE_ERR_UNSUPPORTED       # beyond the medium-batch cap
+    assert _decode(lib, B=9) == F.FLINT_MOE_ERR_WORKSPACE          # 9..64 tokens need the medium workspace
+    assert _decode(lib, B=9, d=F.dims(F.W_BF16), L=_layer(tensor_scales=None)) == F.FLINT_MOE_ERR_UNSUPPORTED
     assert _decode(lib, B=0) == F.FLINT_MOE_ERR_INVALID_ARG
     assert _decode(lib, x=None) == F.FLINT_MOE_ERR_INVALID_ARG
     assert _decode(lib, x=FAKE + 1032) == F.FLINT_MOE_ERR_INVALID_ARG  # not 16-byte aligned
@@ -104,9 +108,12 @@ def test_stack_and_pack_reject_bad_arguments_on_host(lib):
     rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 0, FAKE + 1024, 1, FAKE + 2048, None, None, None,
                                     FAKE + 4096, ws_b, None)
     assert rc == F.FLINT_MOE_ERR_INVALID_ARG
-    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 1, FAKE + 1024, 12, FAKE + 2048, None, None, None,
+    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 1, FAKE + 1024, 65, FAKE + 2048, None, None, None,
                                     FAKE + 4096, ws_b, None)
     assert rc == F.FLINT_MOE_ERR_UNSUPPORTED
+    rc = lib.flint_moe_decode_stack(ctypes.byref(d), arr, 1, FAKE + 1024, 12, FAKE + 2048, None, None, None,
+                                    FAKE + 4096, ws_b, None)
+    assert rc == F.FLINT_MOE_ERR_WORKSPACE  # 12 tokens need the medium-batch workspace
     # NVFP4 pack needs both scale tensors; BF16 pack must not get any
     rc = lib.flint_moe_pack_weights(ctypes.byref(d), FAKE, None, FAKE + 256, FAKE + 512, FAKE + 1024,
                                     F.packed_bytes(), None)
