@@ -61,6 +61,12 @@ enum { FLINT_MOE_W_NVFP4 = 0, FLINT_MOE_W_BF16 = 1 };
  * low-latency path serves up to 8 requests). */
 #define FLINT_MOE_MAX_DECODE_BATCH 8
 
+/* Largest batch of the decode calls.  9..64 tokens (NVFP4 weights only) take
+ * the medium-batch kernels: past the low-latency cap of 8 requests, each
+ * selected expert's weights are read once per group of up to 16 of the
+ * tokens that chose it, instead of once per group of 8 tokens. */
+#define FLINT_MOE_MAX_MEDIUM_BATCH 64
+
 /* Decode kernels for NVFP4 weights (flint_moe_set_decode_kernel). */
 enum { FLINT_MOE_DECODE_CHAINED = 0, FLINT_MOE_DECODE_PERSISTENT = 1 };
 
@@ -91,8 +97,9 @@ typedef struct {
  * Returns 0 for unsupported dims. */
 size_t flint_moe_packed_bytes(const flint_moe_dims *dims);
 
-/* Workspace bytes for calls with at most `max_tokens` tokens
- * (decode: 1..8; prefill: any T >= 1).  Returns 0 for unsupported dims. */
+/* Workspace bytes for calls with at most `max_tokens` tokens (decode: 1..64,
+ * of which 9..64 NVFP4 only; prefill: any T >= 1).  Returns 0 for
+ * unsupported dims or token counts. */
 size_t flint_moe_workspace_bytes(const flint_moe_dims *dims, int max_tokens);
 
 /*
@@ -117,7 +124,7 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
                            size_t packed_bytes, flint_moe_stream_t stream);
 
 /*
- * One MoE sublayer for a decode batch of 1..8 independent tokens.
+ * One MoE sublayer for a decode batch of 1..64 independent tokens.
  *   x        bf16 [B][H] input (RMSNorm'd first if layer->norm_w != NULL)
  *   y        bf16 [B][H] output
  *   topk_ids int32 [B][6] selected experts (descending score) or NULL
@@ -129,9 +136,16 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
  * with FLINT_MOE_DECODE_PERSISTENT selected (flint_moe_set_decode_kernel),
  * NVFP4 weights take one cooperative kernel, one thread block per SM (at
  * least 128 SMs, else FLINT_MOE_ERR_UNSUPPORTED), whose blocks exchange
- * logits, h and y through the workspace.  B > 8 returns
- * FLINT_MOE_ERR_UNSUPPORTED.  The result is deterministic: the same inputs
- * and kernel choice give the same bits on every call.
+ * logits, h and y through the workspace.  9 <= B <= 64 (NVFP4 only, else
+ * FLINT_MOE_ERR_UNSUPPORTED) runs the medium-batch chain: the router over
+ * chunks of 8 tokens; one block that builds the table of slot-chunks (an
+ * expert with up to 16 of the tokens that selected it); gate/up and down
+ * kernels that stream each selected expert's tiles once per slot-chunk; and
+ * a kernel that adds the pairs' down projections in a fixed order.  Its
+ * workspace is flint_moe_workspace_bytes(dims, 64) bytes (less returns
+ * FLINT_MOE_ERR_WORKSPACE).  B > 64 returns FLINT_MOE_ERR_UNSUPPORTED.  The
+ * result is deterministic: the same inputs and kernel choice give the same
+ * bits on every call.
  */
 int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *layer,
                            const void *x, int B, void *y, int32_t *topk_ids,
@@ -146,8 +160,9 @@ int flint_moe_decode_layer(const flint_moe_dims *dims, const flint_moe_layer *la
  *   ids_per_layer   int32 [n_layers][B][6] or NULL
  *   w_per_layer     fp32  [n_layers][B][6] or NULL
  *   ys_per_layer    bf16  [n_layers][B][H] every sublayer's output, or NULL
- * Chained kernels (the default, and BF16 weights): the chain of 3*n_layers
- * kernels is captured once into a CUDA graph (cached per argument set; see
+ * Chained kernels (the default, BF16 weights, and every 9..64-token batch):
+ * the chain of 3 (5 past 8 tokens) kernels per sublayer is captured once
+ * into a CUDA graph (cached per argument set; see
  * flint_moe_release) and replayed with one graph launch per call; the graph
  * bakes in every pointer, so buffer contents may change between calls,
  * addresses not.  Persistent kernel (NVFP4, flint_moe_set_decode_kernel): one

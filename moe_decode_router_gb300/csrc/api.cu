@@ -177,6 +177,7 @@ constexpr int PREFILL_MAX_TOKENS = 1 << 20;
 // In host code its name is only a stand-in; kernels get the device address
 // looked up below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FLINT_MOE_NOALLOC_SCRATCH_BYTES];
+static_assert(MT_MAX == FLINT_MOE_MAX_MEDIUM_BATCH && BMAX == FLINT_MOE_MAX_DECODE_BATCH, "batch caps");
 static_assert(decode_path_ws_bytes() <= FLINT_MOE_NOALLOC_SCRATCH_BYTES,
               "the built-in scratch must hold the decode workspace of 8 tokens");
 
