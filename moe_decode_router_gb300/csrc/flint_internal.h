@@ -125,14 +125,13 @@ struct MediumWs {
   int* xh_exp;       // [64]
   MedRoute* rt;
   void* h;           // bf16 [MPAIRS][512]
-  unsigned* hmax;    // [MPAIRS] fp32 bits of max |h|
   float* part;       // [MPAIRS][2048] scaled down-projection of each pair
   void* y_mid;       // bf16 [64][2048] output of a non-final stack sublayer
 };
 constexpr size_t medium_ws_bytes() {
   return ws_align256((size_t)MT_MAX * E * 2) + ws_align256((size_t)MT_MAX * H * 2) +
          2 * ws_align256((size_t)(MT_MAX / 8) * 8 * 32 * 32 * 4) + ws_align256(MT_MAX * 4) +
-         ws_align256(sizeof(MedRoute)) + ws_align256((size_t)MPAIRS * I * 2) + ws_align256(MPAIRS * 4) +
+         ws_align256(sizeof(MedRoute)) + ws_align256((size_t)MPAIRS * I * 2) +
          ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2);
 }
 MediumWs carve_medium_ws(void* ws);

@@ -20,10 +20,11 @@
 //   mgateup_kernel  items (slot-chunk, 16-row gate/up tile); each CTA walks a
 //                   contiguous range of items, so the activations of a
 //                   slot-chunk are loaded once per CTA; h = bf16(silu(g) * u)
-//                   per pair, with the largest |h| of each pair.
+//                   per pair.
 //   mdown_kernel    items (slot-chunk, 64 output rows); h in f16 scaled by a
-//                   per-pair power of two; writes the pair's down projection
-//                   times its tensor scale, in fp32.
+//                   per-pair power of two (from the pair's largest |h|, which
+//                   the two K-half warps of a row tile find together); writes
+//                   the pair's down projection times its tensor scale, fp32.
 //   mcombine_kernel y = bf16(sum_j w_j d_j + d_shared), j in selection order.
 #include "decode_common.cuh"
 #include "flint_internal.h"
@@ -40,7 +41,6 @@ struct MRouteParams {
   const __nv_bfloat16* logits;  // [T][E]
   int T;
   MedRoute* rt;
-  unsigned* hmax;               // [7T], zeroed here
   int32_t* ids_out;             // [T][6] or null
   float* w_out;                 // [T][6] or null
 };
@@ -158,7 +158,6 @@ __global__ void __launch_bounds__(MR_THREADS, 1) mroute_kernel(const MRouteParam
     if (p.ids_out) p.ids_out[q] = s_ids[t][j];
     if (p.w_out) p.w_out[q] = s_w[t][j];
   }
-  for (int q = tid; q < T * (TOPK + 1); q += MR_THREADS) p.hmax[q] = 0u;
 }
 
 // ------------------------------------------------------------------ common item walk
@@ -176,8 +175,9 @@ constexpr int M_TILE = 18432;  // one item's weights: 16 gate/up rows or 64 down
 static_assert(M_TILE == F4_GU_TILE && M_TILE == 4 * F4_DN_TILE, "item size");
 constexpr int MG_STAGES = 8;
 constexpr int MG_CW = 8;                      // compute warps
-constexpr int MG_RED = 4;                     // partial-sum ring depth
-constexpr int MG_THREADS = 32 * (MG_CW + 1 + 2);  // + producer + 2 epilogue warps
+constexpr int MG_EW = 4;                      // epilogue warps
+constexpr int MG_RED = MG_EW;                 // partial-sum ring: buffer q belongs to epilogue warp q
+constexpr int MG_THREADS = 32 * (MG_CW + 1 + MG_EW);  // + producer
 constexpr int MD_THREADS = 32 * (MG_CW + 1);
 constexpr int TS_WORDS = ((NE * 2 + 3) / 4) * 4;
 
@@ -219,7 +219,6 @@ struct MGateUpParams {
   const int* xh_exp;        // [T]
   const MedRoute* rt;
   __nv_bfloat16* h;         // [pairs][I]
-  unsigned* hmax;           // [pairs]
   unsigned* err;
 };
 
@@ -276,7 +275,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
     }
     for (int b = 0; b < MG_RED; ++b) {
       mbar_init(&rfull[b], MG_CW);
-      mbar_init(&rempty[b], 2);
+      mbar_init(&rempty[b], 1);
     }
     fence_mbar_init();
   }
@@ -293,10 +292,25 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
   }
 
   if (warp < MG_CW) {
-    // ---- compute warps: warp w multiplies K-slice w of every item
+    // ---- compute warps: warp w multiplies K-slice w of every item.  Two
+    // consecutive items of one slot-chunk of at most 8 tokens go through the
+    // interleaved two-slice product (the same bits as two single products).
     uint32_t b0[16][2], b1[16][2];
     int cur = -1, nt = 0;
-    for (int n = 0; lo + n < hi; ++n) {
+    auto hand_over = [&](int n, const float (&a0)[4], const float (&a1)[4]) {
+      const int b = n % MG_RED;
+      if (n >= MG_RED && !mbar_wait(&rempty[b], ((n / MG_RED) - 1) & 1)) atomicOr(p.err, ERR_WAIT_EMPTY);
+      float* rb = red + (size_t)b * 2 * MG_CW * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) rb[warp * 128 + j * 32 + lane] = a0[j];
+      if (nt > 8) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) rb[(MG_CW + warp) * 128 + j * 32 + lane] = a1[j];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[b]);
+    };
+    for (int n = 0; lo + n < hi;) {
       const int i = lo + n, sc = i / GU_TILES, s = n % MG_STAGES;
       if (sc != cur) {
         cur = sc;
@@ -304,6 +318,25 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
         load_x_blocks(p, sc, nt, warp, lane, b0, b1);
       }
       float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+      if (nt <= 8 && lo + n + 1 < hi && (i + 1) / GU_TILES == sc) {
+        const int s1 = (n + 1) % MG_STAGES;
+        const bool ok = mbar_wait(&full[s], (n / MG_STAGES) & 1) && mbar_wait(&full[s1], ((n + 1) / MG_STAGES) & 1);
+        if (ok)
+          nvfp4_slice_mma2(stages + (size_t)s * M_TILE + warp * F4_SLICE, stages + (size_t)s1 * M_TILE + warp * F4_SLICE,
+                           lane, b0, acc0, acc1);
+        else
+          atomicOr(p.err, ERR_WAIT_FULL);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[s]);
+          mbar_arrive(&empty[s1]);
+        }
+        const float z[4] = {0.f, 0.f, 0.f, 0.f};
+        hand_over(n, acc0, z);
+        hand_over(n + 1, acc1, z);
+        n += 2;
+        continue;
+      }
       if (mbar_wait(&full[s], (n / MG_STAGES) & 1)) {
         const uint8_t* sl = stages + (size_t)s * M_TILE + warp * F4_SLICE;
         if (nt > 8)
@@ -315,27 +348,20 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      const int b = n % MG_RED;
-      if (n >= MG_RED && !mbar_wait(&rempty[b], ((n / MG_RED) - 1) & 1)) atomicOr(p.err, ERR_WAIT_EMPTY);
-      float* rb = red + (size_t)b * 2 * MG_CW * 128;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        rb[warp * 128 + j * 32 + lane] = acc0[j];
-        rb[(MG_CW + warp) * 128 + j * 32 + lane] = acc1[j];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&rfull[b]);
+      hand_over(n, acc0, acc1);
+      n += 1;
     }
     return;
   }
 
-  // ---- epilogue warps: thread = (token ep_tk of each block, gate/up row ep_row)
-  const int et = tid - (MG_CW + 1) * 32;
-  const int ep_tk = et >> 3, ep_row = et & 7;
-  const int og = red_off(ep_row, ep_tk), ou = red_off(ep_row + 8, ep_tk);
+  // ---- epilogue warps: warp q takes items n = q (mod MG_EW), whose partial
+  // sums arrive in ring buffer q; lane = (token k = 4 h + lane / 8 for
+  // h = 0..3, gate/up row lane % 8 of the tile).
+  const int q = warp - (MG_CW + 1);
+  const int ep_tk = lane >> 3, ep_row = lane & 7;
   int cur = -1, nt = 0, pair0 = 0;
-  float fk[2] = {0.f, 0.f};  // 2^-exponent x gate/up tensor scale of this thread's two tokens
-  for (int n = 0; lo + n < hi; ++n) {
+  float fk[4] = {0.f, 0.f, 0.f, 0.f};  // 2^-exponent x gate/up tensor scale of tokens 4 h + ep_tk
+  for (int n = q; lo + n < hi; n += MG_EW) {
     const int i = lo + n, sc = i / GU_TILES, tile = i % GU_TILES;
     if (sc != cur) {  // before the wait: the table reads overlap the tile's arithmetic
       cur = sc;
@@ -343,43 +369,37 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
       pair0 = __ldcg(&p.rt->sc_pair[sc]);
       const float ts = ts_s[2 * __ldcg(&p.rt->sc_e[sc])];
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb) {
-        const int k = 8 * bb + ep_tk;
-        fk[bb] = k < nt ? __fmul_rn(exp2i(-__ldcg(p.xh_exp + __ldcg(&p.rt->sc_tok[sc][k]))), ts) : 0.f;
+      for (int h = 0; h < 4; ++h) {
+        const int k = 4 * h + ep_tk;
+        fk[h] = k < nt ? __fmul_rn(exp2i(-__ldcg(p.xh_exp + __ldcg(&p.rt->sc_tok[sc][k]))), ts) : 0.f;
       }
     }
-    const int b = n % MG_RED;
-    if (!mbar_wait(&rfull[b], (n / MG_RED) & 1)) {
+    if (!mbar_wait(&rfull[q], (n / MG_EW) & 1)) {
       atomicOr(p.err, ERR_WAIT_FULL);
       break;
     }
-    const float* rb = red + (size_t)b * 2 * MG_CW * 128;
+    const float* rb = red + (size_t)q * 2 * MG_CW * 128;
 #pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      const int k = 8 * bb + ep_tk;
-      float hm = 0.f;
+    for (int h = 0; h < 4; ++h) {
+      const int k = 4 * h + ep_tk;
       if (k < nt) {
+        const int bb = k >> 3;
+        const int og = red_off(ep_row, k & 7), ou = red_off(ep_row + 8, k & 7);
         float gsum = 0.f, usum = 0.f;
 #pragma unroll
         for (int w = 0; w < MG_CW; ++w) {
           gsum += rb[(bb * MG_CW + w) * 128 + og];
           usum += rb[(bb * MG_CW + w) * 128 + ou];
         }
-        const float f = fk[bb];
-        const float gate = __fmul_rn(gsum, f);
-        const float up = __fmul_rn(usum, f);
+        const float gate = __fmul_rn(gsum, fk[h]);
+        const float up = __fmul_rn(usum, fk[h]);
         const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
         const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
         p.h[(size_t)(pair0 + k) * I + tile * 8 + ep_row] = hv;
-        hm = fabsf(__bfloat162float(hv));
       }
-      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 1));
-      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 2));
-      hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 4));
-      if (ep_row == 0 && k < nt && hm > 0.f) atomicMax(p.hmax + pair0 + k, __float_as_uint(hm));
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&rempty[b]);
+    if (lane == 0) mbar_arrive(&rempty[q]);
   }
 }
 
@@ -390,62 +410,83 @@ struct MDownParams {
   const float* tscale;
   const MedRoute* rt;
   const __nv_bfloat16* h;   // [pairs][I]
-  const unsigned* hmax;     // [pairs]
   float* part;              // [pairs][H]
   unsigned* err;
 };
 
 constexpr int MD_BLOCKS = H / 64;  // 64-row items per expert
 
+constexpr int MD_RED_SET = 2 * 4 * 2 * 128;  // floats: [2 items][4 row tiles][2 blocks][128]
+
 __host__ __device__ constexpr size_t mdown_smem_bytes() {
-  // [stages][red 2 x 4 row tiles x 2 blocks x 128][tensor scales][full, empty]
-  return (size_t)MG_STAGES * M_TILE + 2 * 4 * 2 * 128 * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8;
+  // [stages][red 2 sets][tensor scales][full, empty][hx 4 x 2 x 16]
+  return (size_t)MG_STAGES * M_TILE + 2 * MD_RED_SET * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8 + 4 * 2 * 16 * 4;
 }
 
-// h of slot-chunk sc, K half kh, as f16 B fragments scaled by 2^e(pair).
-__device__ __forceinline__ void load_h_blocks(const MDownParams& p, int pair0, int nt, int kh, int lane,
-                                              uint32_t (&b0)[16][2], uint32_t (&b1)[16][2]) {
+// h of slot-chunk sc, K half kh, as f16 B fragments scaled by 2^e(pair), e
+// from the pair's largest |h| over both K halves: each warp takes the maximum
+// of its half, and the two warps of row tile rtile swap them through hx
+// ([4 row tiles][2 halves][16 tokens]) on named barrier 1 + rtile.  ex[bb]:
+// the exponent of this lane's token 8 bb + lane / 4.
+__device__ __forceinline__ void load_h_blocks(const MDownParams& p, int pair0, int nt, int rtile, int kh, int lane,
+                                              unsigned* hx, uint32_t (&b0)[16][2], uint32_t (&b1)[16][2],
+                                              int (&ex)[2]) {
   const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
   for (int bb = 0; bb < 2; ++bb) {
     uint32_t(&b)[16][2] = bb == 0 ? b0 : b1;
     const int k = 8 * bb + g;
+    uint32_t mx = 0u;  // largest |h| so far, as two bf16 magnitudes
     if (k < nt) {
-      const int pr = pair0 + k;
-      const float sc = exp2i(f16_range_exp(__uint_as_float(__ldcg(p.hmax + pr))));
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.h + (size_t)pr * I) + kh * 128 + t4;
-      uint32_t raw[16][2];
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.h + (size_t)(pair0 + k) * I) + kh * 128 + t4;
 #pragma unroll
       for (int kb = 0; kb < 16; ++kb) {
-        raw[kb][0] = __ldcg(src + kb * 8);
-        raw[kb][1] = __ldcg(src + kb * 8 + 4);
+        b[kb][0] = __ldcg(src + kb * 8);
+        b[kb][1] = __ldcg(src + kb * 8 + 4);
       }
 #pragma unroll
-      for (int kb = 0; kb < 16; ++kb)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint32_t v = raw[kb][r];
-          const __half2 hv = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), sc),
-                                               __fmul_rn(__uint_as_float(v & 0xFFFF0000u), sc));
-          b[kb][r] = *reinterpret_cast<const uint32_t*>(&hv);
-        }
+      for (int kb = 0; kb < 16; ++kb) {
+        mx = __vmaxu2(mx, b[kb][0] & 0x7FFF7FFFu);
+        mx = __vmaxu2(mx, b[kb][1] & 0x7FFF7FFFu);
+      }
     } else {
 #pragma unroll
       for (int kb = 0; kb < 16; ++kb) b[kb][0] = b[kb][1] = 0u;
     }
+    mx = max(mx & 0xFFFFu, mx >> 16);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (t4 == 0) hx[(rtile * 2 + kh) * 16 + k] = mx;
+    named_bar_sync(1 + rtile, 64);
+    mx = max(mx, hx[(rtile * 2 + (kh ^ 1)) * 16 + k]);
+    // As fp32 bits (<< 16) the order of non-negative values is that of their bits.
+    ex[bb] = f16_range_exp(__uint_as_float(mx << 16));
+    const float sc = exp2i(ex[bb]);
+#pragma unroll
+    for (int kb = 0; kb < 16; ++kb)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t v = b[kb][r];
+        const __half2 hv = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), sc),
+                                             __fmul_rn(__uint_as_float(v & 0xFFFF0000u), sc));
+        b[kb][r] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
   }
 }
 
 // Warp w: row tile rt = w / 2 of the item's 64 rows, K half kh = w % 2.  The
 // two warps of a row tile meet on named barrier 1 + rt: the kh = 1 warp hands
-// its sums over, the kh = 0 warp adds them and stores.
+// its sums over, the kh = 0 warp adds them and stores.  Buffer sets alternate
+// between exchanges, so a set is rewritten only after the barrier that follows
+// its last read.
 __global__ void __launch_bounds__(MD_THREADS, 1) mdown_kernel(const MDownParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)MG_STAGES * M_TILE);  // [2][4][2][128]
-  float* ts_s = red + 2 * 4 * 2 * 128;
+  float* red = reinterpret_cast<float*>(smem + (size_t)MG_STAGES * M_TILE);  // [2 sets][MD_RED_SET]
+  float* ts_s = red + 2 * MD_RED_SET;
   uint64_t* full = reinterpret_cast<uint64_t*>(ts_s + TS_WORDS);
   uint64_t* empty = full + MG_STAGES;
+  unsigned* hx = reinterpret_cast<unsigned*>(empty + MG_STAGES);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   for (int q = tid; q < NE * 2; q += MD_THREADS) ts_s[q] = __ldg(p.tscale + q);
@@ -473,59 +514,83 @@ __global__ void __launch_bounds__(MD_THREADS, 1) mdown_kernel(const MDownParams 
   uint32_t b0[16][2], b1[16][2];
   int cur = -1, nt = 0, pair0 = 0;
   float fsc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // 2^-e of this lane's output columns
-  for (int n = 0; lo + n < hi; ++n) {
+  for (int n = 0, u = 0; lo + n < hi;) {
     const int i = lo + n, sc = i / MD_BLOCKS, blk = i % MD_BLOCKS, s = n % MG_STAGES;
     if (sc != cur) {
       cur = sc;
       nt = __ldcg(&p.rt->sc_n[sc]);
       pair0 = __ldcg(&p.rt->sc_pair[sc]);
-      load_h_blocks(p, pair0, nt, kh, lane, b0, b1);
+      int ex[2];
+      load_h_blocks(p, pair0, nt, rtile, kh, lane, hx, b0, b1, ex);
       const float ts = ts_s[2 * __ldcg(&p.rt->sc_e[sc]) + 1];
 #pragma unroll
       for (int bb = 0; bb < 2; ++bb)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int k = 8 * bb + 2 * t4 + j;
-          fsc[bb][j] = k < nt ? __fmul_rn(ts, exp2i(-f16_range_exp(__uint_as_float(__ldcg(p.hmax + pair0 + k)))))
-                              : 0.f;
+          const int k = 8 * bb + 2 * t4 + j;  // output column: token of lanes 4 (2 t4 + j) ..
+          const int e = __shfl_sync(0xffffffffu, ex[bb], (2 * t4 + j) * 4);
+          fsc[bb][j] = k < nt ? __fmul_rn(ts, exp2i(-e)) : 0.f;
         }
     }
-    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mbar_wait(&full[s], (n / MG_STAGES) & 1)) {
-      const uint8_t* sl = stages + (size_t)s * M_TILE + (rtile * 2 + kh) * F4_SLICE;
-      if (nt > 8)
-        nvfp4_slice_mma_n16(sl, lane, b0, b1, acc0, acc1);
+    // One exchange between the two warps of the row tile: one item, or two
+    // consecutive items of a slot-chunk of at most 8 tokens through the
+    // interleaved two-slice product.  Exchange u uses buffer set u & 1.
+    const bool two = nt <= 8 && lo + n + 1 < hi && (i + 1) / MD_BLOCKS == sc;
+    const int s1 = (n + 1) % MG_STAGES;
+    const int sl_off = (rtile * 2 + kh) * F4_SLICE;
+    float acc[2][2][4] = {};  // [item][block][4]
+    if (two) {
+      if (mbar_wait(&full[s], (n / MG_STAGES) & 1) && mbar_wait(&full[s1], ((n + 1) / MG_STAGES) & 1))
+        nvfp4_slice_mma2(stages + (size_t)s * M_TILE + sl_off, stages + (size_t)s1 * M_TILE + sl_off, lane, b0,
+                         acc[0][0], acc[1][0]);
       else
-        nvfp4_slice_mma(sl, lane, b0, acc0);
+        atomicOr(p.err, ERR_WAIT_FULL);
+    } else if (mbar_wait(&full[s], (n / MG_STAGES) & 1)) {
+      const uint8_t* sl = stages + (size_t)s * M_TILE + sl_off;
+      if (nt > 8)
+        nvfp4_slice_mma_n16(sl, lane, b0, b1, acc[0][0], acc[0][1]);
+      else
+        nvfp4_slice_mma(sl, lane, b0, acc[0][0]);
     } else {
       atomicOr(p.err, ERR_WAIT_FULL);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
-    float* rb = red + ((size_t)(n & 1) * 4 + rtile) * 2 * 128;
+    if (lane == 0) {
+      mbar_arrive(&empty[s]);
+      if (two) mbar_arrive(&empty[s1]);
+    }
+    const int items = two ? 2 : 1;
+    float* rset = red + (size_t)(u & 1) * MD_RED_SET;  // [2 items][4 row tiles][2 blocks][128]
     if (kh == 1) {
-      *reinterpret_cast<float4*>(rb + lane * 4) = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
-      *reinterpret_cast<float4*>(rb + 128 + lane * 4) = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+      for (int it = 0; it < items; ++it)
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb)
+          *reinterpret_cast<float4*>(rset + ((it * 4 + rtile) * 2 + bb) * 128 + lane * 4) =
+              make_float4(acc[it][bb][0], acc[it][bb][1], acc[it][bb][2], acc[it][bb][3]);
     }
     named_bar_sync(1 + rtile, 64);
     if (kh == 0) {
-      const float4 o0 = *reinterpret_cast<const float4*>(rb + lane * 4);
-      const float4 o1 = *reinterpret_cast<const float4*>(rb + 128 + lane * 4);
-      const float v[2][4] = {{acc0[0] + o0.x, acc0[1] + o0.y, acc0[2] + o0.z, acc0[3] + o0.w},
-                             {acc1[0] + o1.x, acc1[1] + o1.y, acc1[2] + o1.z, acc1[3] + o1.w}};
-      const int row = blk * 64 + rtile * 16 + g;
+      for (int it = 0; it < items; ++it) {
+        const int row = (blk + it) * 64 + rtile * 16 + g;
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
+        for (int bb = 0; bb < 2; ++bb) {
+          const float4 o = *reinterpret_cast<const float4*>(rset + ((it * 4 + rtile) * 2 + bb) * 128 + lane * 4);
+          const float v[4] = {acc[it][bb][0] + o.x, acc[it][bb][1] + o.y, acc[it][bb][2] + o.z,
+                              acc[it][bb][3] + o.w};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int k = 8 * bb + 2 * t4 + j;
-          if (k < nt) {
-            float* dst = p.part + (size_t)(pair0 + k) * H + row;
-            dst[0] = __fmul_rn(v[bb][j], fsc[bb][j]);
-            dst[8] = __fmul_rn(v[bb][2 + j], fsc[bb][j]);
+          for (int j = 0; j < 2; ++j) {
+            const int k = 8 * bb + 2 * t4 + j;
+            if (k < nt) {
+              float* dst = p.part + (size_t)(pair0 + k) * H + row;
+              dst[0] = __fmul_rn(v[j], fsc[bb][j]);
+              dst[8] = __fmul_rn(v[2 + j], fsc[bb][j]);
+            }
           }
         }
+      }
     }
+    n += items;
+    ++u;
   }
 }
 
@@ -598,8 +663,6 @@ MediumWs carve_medium_ws(void* ws) {
   q += ws_align256(sizeof(MedRoute));
   w.h = q;
   q += ws_align256((size_t)MPAIRS * I * 2);
-  w.hmax = reinterpret_cast<unsigned*>(q);
-  q += ws_align256(MPAIRS * 4);
   w.part = reinterpret_cast<float*>(q);
   q += ws_align256((size_t)MPAIRS * H * 4);
   w.y_mid = q;
@@ -608,8 +671,7 @@ MediumWs carve_medium_ws(void* ws) {
 static_assert(medium_ws_bytes() == ws_align256((size_t)MT_MAX * E * 2) + ws_align256((size_t)MT_MAX * H * 2) +
                                        2 * ws_align256((size_t)(MT_MAX / 8) * XFRAG_WORDS_M * 4) +
                                        ws_align256(MT_MAX * 4) + ws_align256(sizeof(MedRoute)) +
-                                       ws_align256((size_t)MPAIRS * I * 2) + ws_align256(MPAIRS * 4) +
-                                       ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2),
+                                       ws_align256((size_t)MPAIRS * I * 2) + ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2),
               "medium workspace size and carve-up must agree");
 
 cudaError_t medium_kernels_init() {
@@ -629,7 +691,6 @@ cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float 
   rp.logits = static_cast<const __nv_bfloat16*>(ws.logits);
   rp.T = T;
   rp.rt = ws.rt;
-  rp.hmax = ws.hmax;
   rp.ids_out = ids_out;
   rp.w_out = w_out;
   if ((e = launch_pdl(mroute_kernel, 1, MR_THREADS, 0, st, true, rp)) != cudaSuccess) return e;
@@ -641,7 +702,6 @@ cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float 
   gp.xh_exp = ws.xh_exp;
   gp.rt = ws.rt;
   gp.h = static_cast<__nv_bfloat16*>(ws.h);
-  gp.hmax = ws.hmax;
   gp.err = err;
   if ((e = launch_pdl(mgateup_kernel, sm_count, MG_THREADS, mgateup_smem_bytes(), st, true, gp)) != cudaSuccess)
     return e;
@@ -651,7 +711,6 @@ cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float 
   dp.tscale = L.tscale;
   dp.rt = ws.rt;
   dp.h = gp.h;
-  dp.hmax = ws.hmax;
   dp.part = ws.part;
   dp.err = err;
   if ((e = launch_pdl(mdown_kernel, sm_count, MD_THREADS, mdown_smem_bytes(), st, true, dp)) != cudaSuccess)
