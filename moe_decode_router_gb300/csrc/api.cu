@@ -257,7 +257,8 @@ size_t flint_moe_workspace_bytes(const flint_moe_dims* dims, int max_tokens) {
   if (dims->weight_dtype != FLINT_MOE_W_NVFP4) return max_tokens <= BMAX ? dec : 0;  // medium, prefill: NVFP4 only
   size_t n = prefill_ws_bytes(max_tokens);
   if (n < dec) n = dec;
-  if (max_tokens > BMAX && max_tokens <= MT_MAX && n < medium_ws_bytes()) n = medium_ws_bytes();
+  // Any decode call of 9..64 tokens is a call of at most max_tokens tokens.
+  if (max_tokens > BMAX && n < medium_ws_bytes()) n = medium_ws_bytes();
   return n;
 }
 

@@ -44,6 +44,7 @@ def test_packed_and_workspace_sizes(lib):
     assert ws > 0 and ws % 256 == 0
     assert F.workspace_bytes(F.W_NVFP4, 1) == ws
     assert F.workspace_bytes(F.W_NVFP4, 64) > ws                   # medium-batch tables, h and partials
+    assert F.workspace_bytes(F.W_NVFP4, 65) >= F.workspace_bytes(F.W_NVFP4, 64)  # covers every smaller call
     assert F.workspace_bytes(F.W_BF16, 9) == 0                     # 9..64 tokens: NVFP4 only
     bad = F.Dims(4096, 256, 1, 512, 6, 0, 1e-6)
     assert lib.flint_moe_packed_bytes(ctypes.byref(bad)) == 0
