@@ -57,6 +57,8 @@ WORKLOADS = {
     "stack47_b16_nvfp4": dict(cfg=2, batch=16, fmt="nvfp4"),  # medium-batch path (9..64 tokens)
     "stack47_b64_nvfp4": dict(cfg=2, batch=64, fmt="nvfp4"),
     "prefill8192_nvfp4": dict(cfg=4, batch=8192, fmt="nvfp4", prefill=True),
+    "dense_gemv_b1_nvfp4": dict(dense=True, batch=1, fmt="nvfp4"),  # 8192 x 2048 packed NVFP4 GEMV
+    "dense_gemv_b8_nvfp4": dict(dense=True, batch=8, fmt="nvfp4"),
 }
 METRIC = "MoE decode µs/layer & effective HBM GB/s (% of roofline) at batch 1 and 8"
 
@@ -72,6 +74,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="measure only --workload")
+    ap.add_argument("--decode-kernel", default="chained", choices=["chained", "persistent"],
+                    help="NVFP4 decode kernels of a 1..8-token --workload")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -86,6 +90,10 @@ def dist_env():
 def workload_config(name: str, world: int, layers: int = N_LAYERS) -> dict:
     """The `config` object of a workload; both arms print exactly this."""
     wl = WORKLOADS[name]
+    if wl.get("dense"):
+        return {"workload": name, "batch": wl["batch"], "N": DENSE_N, "K": DENSE_K, "matrices": DENSE_MATS,
+                "weights": "nvfp4", "parallelism": f"replicas x{world}",
+                "l2": f"{DENSE_MATS} distinct matrices cycled (444 MB): larger than L2"}
     if wl.get("prefill"):
         return {"workload": name, "tokens": wl["batch"], "hidden": 2048, "experts": "256+1", "inter": 512,
                 "top_k": 6, "weights": wl["fmt"], "parallelism": f"replicas x{world}",
@@ -127,6 +135,43 @@ while True:
 dt = time.perf_counter() - t0
 print(json.dumps({"layers": n, "seconds": dt}), flush=True)
 """
+
+
+_DENSE_CHILD = r"""
+import json, sys, time, os
+sys.path.insert(0, os.environ["FLINT_ROOT"])
+import numpy as np, torch
+torch.set_num_threads(1)
+import oracle as O, synth
+N, K, batch, budget = int(sys.argv[1]), int(sys.argv[2]), int(sys.argv[3]), float(sys.argv[4])
+d = synth.gen_dense(N, K, index=0, device="cpu")
+codes, scales = d["codes"].numpy(), d["scales"].numpy()
+x = O.bf16_bits_to_f64(synth.gen_dense_x(batch, K, index=0).view(torch.int16).numpy().view(np.uint16))
+n = 0
+t0 = time.perf_counter()
+while True:
+    O.dense_gemv(x, codes, scales, d["tensor_scale"])
+    n += 1
+    if time.perf_counter() - t0 >= budget and n >= 2:
+        break
+print(json.dumps({"calls": n, "seconds": time.perf_counter() - t0}), flush=True)
+"""
+
+
+def time_oracle_dense(batch: int, budget_s: float) -> dict:
+    """The oracle's dense GEMV (dequantise the whole matrix, fp64 product) on one
+    8192 x 2048 matrix, single-threaded, for about budget_s seconds: us per call."""
+    env = dict(os.environ)
+    env.update(FLINT_ROOT=ROOT, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _DENSE_CHILD, str(DENSE_N), str(DENSE_K), str(batch), str(budget_s)],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return dict(value=1e6 * res["seconds"] / res["calls"], unit="us/call", cores=1, kind="oracle",
+                sample=f"{res['calls']} calls of the {DENSE_N}x{DENSE_K} dense GEMV at batch {batch}, one "
+                       f"single-threaded numpy fp64 process, {res['seconds']:.1f} s")
 
 
 def time_oracle(cfg: int, batch: int, fmt: str, budget_s: float, procs: int = 1) -> dict:
@@ -283,10 +328,14 @@ SOURCES = {
     "fused": [CSRC + "decode_fused.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
     "chain": [CSRC + "decode.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
     "prefill": [CSRC + "prefill.cu", CSRC + "tc05.cuh", CSRC + "flint_common.cuh"],
+    "medium": [CSRC + "medium.cu", CSRC + "decode.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
+    "dense": [CSRC + "dense.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
 }
 TRAFFIC_FILES = {
-    "fused": "profiles/decode_fused_stack_b1_b8.md",
-    "chain": "profiles/decode_chain_bf16_b8.md",
+    "fused": "profiles/decode_fused_dram.md",
+    "chain": "profiles/decode_chain_dram.md",
+    "medium": "profiles/decode_medium_dram.md",
+    "dense": "profiles/dense_gemv_8192x2048.md",
     "prefill": "profiles/prefill8192_nvfp4_kernels.md",
 }
 
@@ -419,7 +468,7 @@ def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, w
     bytes_per_layer = total_bytes / steps / NL
     F.set_decode_kernel(F.DECODE_CHAINED)
     persistent = persistent and fmt == F.W_NVFP4
-    kind = "fused" if persistent else "chain"
+    kind = "fused" if persistent else ("medium" if B > 8 else "chain")
     prof, prof_src = profiled_traffic(kind, name)
     traffic = round(float(prof["ratio"]) * bytes_per_layer * NL) if prof else None
     launches = math.ceil(NL / FUSED_MAX_LAYERS) if persistent else (5 if B > 8 else 3) * NL
@@ -574,11 +623,13 @@ def measure_dense(F, synth, torch, B: int, steps: int, warmup: int, world: int, 
     nbytes = DENSE_N * DENSE_K * 9 // 16
     gbs = nbytes * world / (us * 1e-6) / 1e9
     peak = read_peaks().get("hbm_gbs") or 6800.0
+    prof, prof_src = profiled_traffic("dense", f"dense_gemv_b{B}_nvfp4")
     return {
         "workload": f"dense_gemv_{DENSE_N}x{DENSE_K}_b{B}_nvfp4", "value": round(us, 3), "unit": "us/call",
         "effective_hbm_gbs": round(gbs, 1),
         "roofline": {"kernel": "dense_gemv_kernel", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(gbs / peak, 4), "bytes_per_call": nbytes, "traffic": None},
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "bytes_per_call": nbytes,
+                     "traffic": int(prof["bytes"]) if prof else None, "traffic_source": prof_src},
         "e2e": {"value": round(e2e_ms * 1000.0, 3), "unit": "us/call", "h2d_bytes_per_step": B * DENSE_K * 2,
                 "d2h_bytes_per_step": B * DENSE_N * 2},
         "gpu_launches": calls, "timing": "CUDA graph of 47 calls (one per distinct matrix), replayed",
@@ -608,11 +659,15 @@ def run_ours(args):
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
 
     extras = {}
-    if wl.get("prefill"):
+    if wl.get("dense"):
+        res = measure_dense(F, synth, torch, wl["batch"], args.steps, args.warmup, world, dev, local)
+        res["ms_per_step"] = round(res["value"] / 1000.0, 6)
+    elif wl.get("prefill"):
         res = measure_prefill(F, synth, torch, name, args.steps, args.warmup, world, dev, local)
     else:
         layers = build_stack(F, synth, torch, wl["fmt"], dev, args.layers)
-        res = measure_stack(F, synth, torch, name, layers, args.steps, args.warmup, world, dev, local)
+        res = measure_stack(F, synth, torch, name, layers, args.steps, args.warmup, world, dev, local,
+                            persistent=args.decode_kernel == "persistent" and wl["batch"] <= 8)
         if name == "stack47_b1_nvfp4" and not args.no_extras:
             # batch 8 on the same resident weights, and both batches on the persistent kernel
             extras["batch8"] = dict(workload="stack47_b8_nvfp4", **measure_stack(
@@ -651,7 +706,7 @@ def run_ours(args):
     out = {
         "metric": METRIC,
         "value": res["value"],
-        "unit": "us/layer",
+        "unit": res.get("unit", "us/layer"),
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -666,7 +721,9 @@ def run_ours(args):
     out.update({k: v for k, v in res.items() if k not in ("value", "unit", "ms_per_step")})
     if want_cpu:
         try:
-            if wl.get("prefill"):
+            if wl.get("dense"):
+                out["cpu_baseline"] = time_oracle_dense(wl["batch"], args.cpu_seconds)
+            elif wl.get("prefill"):
                 out["cpu_baseline"] = time_oracle_prefill(wl["cfg"], wl["batch"])
             else:
                 out["cpu_baseline"] = time_oracle_all(wl["cfg"], wl["batch"], wl["fmt"], args.cpu_seconds)
@@ -706,6 +763,15 @@ def run_reference(args):
         "data": "synthetic (seeded generator, random-init weights of the Flint MoE shapes)",
         "config": workload_config(name, world, args.layers),
     }
+    if wl.get("dense"):
+        r = time_oracle_dense(wl["batch"], max(1.0, min(60.0, 2.0 * max(1, args.steps))))
+        us = r["value"]
+        common["unit"] = "us/call"
+        print(json.dumps(dict(common, value=round(us, 1), steps=args.steps, warmup=0,
+                              ms_per_step=round(us / 1000.0, 3), cpu_baseline=r,
+                              e2e={"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                                   "d2h_bytes_per_step": 0})), flush=True)
+        return
     if wl.get("prefill"):
         r = time_oracle_prefill(wl["cfg"], wl["batch"])
         us = r["value"]
