@@ -514,10 +514,10 @@ struct DnCfg {
 
 template <int FMT, int STAGES, int NG>
 __host__ __device__ constexpr size_t down_smem_fixed() {
-  // [stages][red (2NG) x 128 fp32][tensor scales][full, empty barriers][hexp 8, misc 8 ints][pidx]
-  // [pair token][pair slot][Routing]
+  // [stages][red (2NG) x 128 fp32][tensor scales][full, empty barriers, h barrier][hexp 8, misc 8 ints]
+  // [pidx][pair token][pair slot][Routing]
   return (size_t)STAGES * Fmt<FMT>::DN_TILE + DnCfg<NG>::COMPUTE_WARPS * 128 * 4 + TSCALE_WORDS * 4 +
-         2 * STAGES * 8 + 64 + MAX_SLOTS * BMAX + 64 + 64 + sizeof(Routing);
+         2 * STAGES * 8 + 8 + 64 + MAX_SLOTS * BMAX + 64 + 64 + sizeof(Routing);
 }
 template <int FMT, int STAGES, int NG>
 size_t down_smem_bytes(int B) {
@@ -541,7 +541,8 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   float* ts_s = red + NCW * 128;                                         // [NE][2]
   uint64_t* full = reinterpret_cast<uint64_t*>(ts_s + TSCALE_WORDS);
   uint64_t* empty = full + STAGES;
-  int* hexp = reinterpret_cast<int*>(empty + STAGES);    // [8]
+  uint64_t* hbar = empty + STAGES;                       // the staged h rows
+  int* hexp = reinterpret_cast<int*>(hbar + 1);          // [8]
   int* misc = hexp + 8;                                  // [1] n_pairs
   uint8_t* pidx = reinterpret_cast<uint8_t*>(misc + 8);  // [MAX_SLOTS][8]
   uint8_t* psrc_tok = pidx + MAX_SLOTS * BMAX;           // [<= 56] token of pair
@@ -571,6 +572,7 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 2);
     }
+    mbar_init(hbar, 1);
     fence_mbar_init();
   }
   zero_routing(R, tid, NT);
@@ -629,12 +631,14 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
 
-  // One round trip: every h row chunk is requested at once, together with the
-  // per-token maxima that set the f16 exponents.
-  for (int idx = tid; idx < n_pairs * 64; idx += NT) {
-    const int pr = idx >> 6, ch = idx & 63;
-    const int tk = psrc_tok[pr], u = psrc_slot[pr];
-    cp_async16(hs + (size_t)pr * HS_STRIDE + ch * 8, p.h + ((size_t)u * BMAX + tk) * I + ch * 8);
+  // One round trip: every h row is requested at once, one bulk copy per pair,
+  // together with the per-token maxima that set the f16 exponents.
+  if (tid == NCW * 32) {
+    const uint64_t hpol = l2_evict_last();
+    mbar_arrive_expect_tx(hbar, (uint32_t)(n_pairs * I * 2));
+    for (int pr = 0; pr < n_pairs; ++pr)
+      bulk_g2s(hs + (size_t)pr * HS_STRIDE, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I, I * 2, hbar,
+               hpol);
   }
   if (FMT == 0 && warp < B) {
     float v[MAX_HPARTS / 32];
@@ -649,7 +653,7 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
     const unsigned mb = redux_max(__float_as_uint(m));
     if (lane == 0) hexp[warp] = f16_range_exp(__uint_as_float(mb));
   }
-  cp_async_wait_all();
+  if (!mbar_wait(hbar, 0) && tid == 0) atomicOr(p.err, ERR_WAIT_FULL);
   __syncthreads();
   if (FMT == 0) {
     // bf16 h -> f16 h * 2^hexp[token], in place (each thread its own chunks).
@@ -671,8 +675,15 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   }
 
   if (warp == NCW) {
-    if (lane == 0) {
-      for (int n = issued; n < n_slots; ++n) {
+    if (lane < NG) {
+      // Lane j serves the slots u = j (mod NG): their stages are freed by
+      // consumer group j alone, so the lanes wait on their groups in parallel
+      // instead of one thread waking once per tile.  The prologue (lane 0,
+      // before the dependency wait) requested slots 0 .. min(STAGES, n_slots) - 1.
+      const int pro = n_slots < STAGES ? n_slots : STAGES;
+      int n = lane;
+      while (n < pro) n += NG;
+      for (; n < n_slots; n += NG) {
         const int s = n % STAGES;
         if (!mbar_wait(&empty[s], ((n / STAGES) - 1) & 1)) {
           atomicOr(p.err, ERR_WAIT_EMPTY);
@@ -682,12 +693,11 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
         mbar_arrive_expect_tx(&full[s], TILE);
         bulk_g2s(stages + (size_t)s * TILE, p.experts + (size_t)e * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE,
                  TILE, &full[s], pol);
-        issued = n + 1;
       }
-      for (int n = issued - STAGES; n < issued; ++n) {
-        if (n < 0) continue;
-        if (!mbar_wait(&full[n % STAGES], (n / STAGES) & 1)) atomicOr(p.err, ERR_DRAIN);
-      }
+      // Do not leave copies in flight: this lane's last STAGES / NG slots
+      // (earlier ones had their stage reused, so they have landed).
+      for (int m = n - NG; m >= 0 && m > n - NG - STAGES; m -= NG)
+        if (!mbar_wait(&full[m % STAGES], (m / STAGES) & 1)) atomicOr(p.err, ERR_DRAIN);
     }
     return;
   }
