@@ -506,6 +506,8 @@ struct DownParams {
 
 constexpr int MAX_HPARTS = 512;
 
+constexpr int DN_BULK_H_MAX = 16;  // staged h rows up to which they come by bulk copies
+
 template <int NG>
 struct DnCfg {
   static constexpr int COMPUTE_WARPS = 2 * NG;  // NG slot groups x 2 K halves
@@ -631,14 +633,24 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
 
-  // One round trip: every h row is requested at once, one bulk copy per pair,
-  // together with the per-token maxima that set the f16 exponents.
-  if (tid == NCW * 32) {
-    const uint64_t hpol = l2_evict_last();
-    mbar_arrive_expect_tx(hbar, (uint32_t)(n_pairs * I * 2));
-    for (int pr = 0; pr < n_pairs; ++pr)
-      bulk_g2s(hs + (size_t)pr * HS_STRIDE, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I, I * 2, hbar,
-               hpol);
+  // One round trip: every h row is requested at once, together with the
+  // per-token maxima that set the f16 exponents.  A few rows go as one bulk
+  // copy each; with many, the copy engine's per-copy cost would dominate, so
+  // every thread requests 16-byte pieces instead.
+  const bool h_bulk = n_pairs <= DN_BULK_H_MAX;
+  if (h_bulk) {
+    if (tid == NCW * 32) {
+      const uint64_t hpol = l2_evict_last();
+      mbar_arrive_expect_tx(hbar, (uint32_t)(n_pairs * I * 2));
+      for (int pr = 0; pr < n_pairs; ++pr)
+        bulk_g2s(hs + (size_t)pr * HS_STRIDE, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I, I * 2, hbar,
+                 hpol);
+    }
+  } else {
+    for (int idx = tid; idx < n_pairs * 64; idx += NT) {
+      const int pr = idx >> 6, ch = idx & 63;
+      cp_async16(hs + (size_t)pr * HS_STRIDE + ch * 8, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I + ch * 8);
+    }
   }
   if (FMT == 0 && warp < B) {
     float v[MAX_HPARTS / 32];
@@ -653,7 +665,11 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
     const unsigned mb = redux_max(__float_as_uint(m));
     if (lane == 0) hexp[warp] = f16_range_exp(__uint_as_float(mb));
   }
-  if (!mbar_wait(hbar, 0) && tid == 0) atomicOr(p.err, ERR_WAIT_FULL);
+  if (h_bulk) {
+    if (!mbar_wait(hbar, 0) && tid == 0) atomicOr(p.err, ERR_WAIT_FULL);
+  } else {
+    cp_async_wait_all();
+  }
   __syncthreads();
   if (FMT == 0) {
     // bf16 h -> f16 h * 2^hexp[token], in place (each thread its own chunks).
@@ -675,15 +691,18 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   }
 
   if (warp == NCW) {
-    if (lane < NG) {
-      // Lane j serves the slots u = j (mod NG): their stages are freed by
-      // consumer group j alone, so the lanes wait on their groups in parallel
-      // instead of one thread waking once per tile.  The prologue (lane 0,
-      // before the dependency wait) requested slots 0 .. min(STAGES, n_slots) - 1.
+    // NVFP4: lane j serves the slots u = j (mod NG), whose stages consumer
+    // group j alone frees, so the lanes wait on their groups in parallel
+    // instead of one thread waking once per 4.6 KB tile.  BF16 (16 KB tiles,
+    // one stage per group): one lane in slot order was measured faster.
+    constexpr int PL = FMT == 0 ? NG : 1;
+    if (lane < PL) {
+      // The prologue (lane 0, before the dependency wait) requested slots
+      // 0 .. min(STAGES, n_slots) - 1.
       const int pro = n_slots < STAGES ? n_slots : STAGES;
       int n = lane;
-      while (n < pro) n += NG;
-      for (; n < n_slots; n += NG) {
+      while (n < pro) n += PL;
+      for (; n < n_slots; n += PL) {
         const int s = n % STAGES;
         if (!mbar_wait(&empty[s], ((n / STAGES) - 1) & 1)) {
           atomicOr(p.err, ERR_WAIT_EMPTY);
@@ -694,9 +713,9 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
         bulk_g2s(stages + (size_t)s * TILE, p.experts + (size_t)e * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE,
                  TILE, &full[s], pol);
       }
-      // Do not leave copies in flight: this lane's last STAGES / NG slots
+      // Do not leave copies in flight: this lane's last STAGES / PL slots
       // (earlier ones had their stage reused, so they have landed).
-      for (int m = n - NG; m >= 0 && m > n - NG - STAGES; m -= NG)
+      for (int m = n - PL; m >= 0 && m > n - PL - STAGES; m -= PL)
         if (!mbar_wait(&full[m % STAGES], (m / STAGES) & 1)) atomicOr(p.err, ERR_DRAIN);
     }
     return;
