@@ -632,6 +632,13 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   }
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
+  if (FMT == 0 && tid == NCW * 32 + 1) {
+    // HBM is idle now: every NVFP4 tile beyond the ring is asked into L2 at
+    // once, so the ring refills at L2 latency (BF16's 16 KB tiles would take
+    // most of L2 at 8 tokens; measured slower there).
+    for (int n = STAGES; n < n_slots; ++n)
+      bulk_prefetch_l2(p.experts + (size_t)R.slot_expert[n] * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE, TILE);
+  }
 
   // One round trip: every h row is requested at once, together with the
   // per-token maxima that set the f16 exponents.  A few rows go as one bulk

@@ -128,6 +128,12 @@ __device__ __forceinline__ uint64_t l2_evict_last() {
   return pol;
 }
 
+// Requests `bytes` at gsrc into L2 (no destination, nothing to wait for).
+// gsrc 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 // One TMA bulk copy global -> shared, completion counted on `bar` in bytes.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar,
