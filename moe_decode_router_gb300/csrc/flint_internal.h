@@ -98,13 +98,13 @@ cudaError_t launch_prefill(const LayerArgs& L, const void* x, int T, float eps, 
                            float* w_out, void* ws, int sm_count, unsigned* err, cudaStream_t st);
 
 // Medium-batch decode path (medium.cu), 9..64 tokens, NVFP4 weights.  Tokens
-// of one expert are processed in slot-chunks of up to MCH tokens (two mma
-// n8 blocks); pairs (token, expert) are numbered expert by expert, the shared
+// of one expert are processed in slot-chunks of up to MCH tokens (one mma n8
+// block); pairs (token, expert) are numbered expert by expert, the shared
 // expert first.
 constexpr int MT_MAX = 64;
-constexpr int MCH = 16;
+constexpr int MCH = 8;
 constexpr int MPAIRS = (TOPK + 1) * MT_MAX;
-constexpr int MSC_MAX = 288;  // >= 257 experts + 7 MT_MAX / MCH extra chunks
+constexpr int MSC_MAX = 320;  // >= 257 experts + 7 MT_MAX / MCH extra chunks
 static_assert(MSC_MAX >= NE + MPAIRS / MCH, "slot-chunk table");
 struct MedRoute {
   int n_sc;                        // slot-chunks

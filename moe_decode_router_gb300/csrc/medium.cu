@@ -6,20 +6,21 @@
 // experts at 64 tokens), so splitting the batch into groups of 8 would read
 // most experts several times (649 MB instead of 355 MB per sublayer at 64
 // tokens).  This path reads every selected expert's weights once per
-// slot-chunk: the tokens of one expert, up to 16 at a time, ride as two mma
-// n8 blocks on each dequantised weight fragment.  Five kernels, chained with
+// slot-chunk: the tokens of one expert, up to 8 at a time, ride as the mma n8
+// block on each dequantised weight fragment.  Five kernels, chained with
 // programmatic dependent launch:
 //
 //   router_kernel   (decode.cu) over chunks of 8 tokens: RMSNorm, bf16
 //                   logits (error-free accumulation), x_hat fragments in f16
 //                   scaled by a per-token power of two.
 //   mroute_kernel   one CTA: sigmoid top-6 per token, then the slot-chunk
-//                   table (expert, up to 16 tokens, first pair) with the
+//                   table (expert, up to 8 tokens, first pair) with the
 //                   shared expert first and the routed experts in ascending
 //                   order, and the pair of every (token, expert).
 //   mgateup_kernel  items (slot-chunk, 16-row gate/up tile); each CTA walks a
-//                   contiguous range of items, so the activations of a
-//                   slot-chunk are loaded once per CTA; h = bf16(silu(g) * u)
+//                   contiguous range of items with two groups of compute
+//                   warps taking alternate items, so the activations of a
+//                   slot-chunk are loaded once per group; h = bf16(silu(g) * u)
 //                   per pair.
 //   mdown_kernel    items (slot-chunk, 64 output rows); h in f16 scaled by a
 //                   per-pair power of two (from the pair's largest |h|, which
@@ -174,10 +175,15 @@ __device__ __forceinline__ void item_range(int n_items, int& lo, int& hi) {
 constexpr int M_TILE = 18432;  // one item's weights: 16 gate/up rows or 64 down rows, all of K
 static_assert(M_TILE == F4_GU_TILE && M_TILE == 4 * F4_DN_TILE, "item size");
 constexpr int MG_STAGES = 8;
-constexpr int MG_CW = 8;                      // compute warps
+constexpr int MG_CW = 8;                      // compute warps of a group (one K-slice each)
+constexpr int MG_GROUPS = 2;                  // gate/up: compute groups taking alternate items
+constexpr int MG_PW = MG_GROUPS * MG_CW;      // gate/up producer warp
 constexpr int MG_EW = 4;                      // epilogue warps
 constexpr int MG_RED = MG_EW;                 // partial-sum ring: buffer q belongs to epilogue warp q
-constexpr int MG_THREADS = 32 * (MG_CW + 1 + MG_EW);  // + producer
+constexpr int MG_THREADS = 32 * (MG_PW + 1 + MG_EW);
+// Item n uses stage n % MG_STAGES and ring buffer n % MG_RED: each belongs to
+// one compute group, which consumes it in order, as the parity waits require.
+static_assert(MG_STAGES % MG_GROUPS == 0 && MG_RED % MG_GROUPS == 0, "stage and buffer ownership");
 constexpr int MD_THREADS = 32 * (MG_CW + 1);
 constexpr int TS_WORDS = ((NE * 2 + 3) / 4) * 4;
 
@@ -223,44 +229,39 @@ struct MGateUpParams {
 };
 
 __host__ __device__ constexpr size_t mgateup_smem_bytes() {
-  // [stages][red MG_RED x 2 blocks x 8 warps x 128][tensor scales][full, empty][rfull, rempty]
-  return (size_t)MG_STAGES * M_TILE + (size_t)MG_RED * 2 * MG_CW * 128 * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8 +
+  // [stages][red MG_RED x 8 warps x 128][tensor scales][full, empty][rfull, rempty]
+  return (size_t)MG_STAGES * M_TILE + (size_t)MG_RED * MG_CW * 128 * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8 +
          2 * MG_RED * 8;
 }
 
-// Activation fragments of slot-chunk sc for K-slice `slice`: block bb holds
-// tokens 8 bb .. 8 bb + 7 of the chunk (zeros past its end).
-__device__ __forceinline__ void load_x_blocks(const MGateUpParams& p, int sc, int nt, int slice, int lane,
-                                              uint32_t (&b0)[16][2], uint32_t (&b1)[16][2]) {
+// Activation fragments of slot-chunk sc for K-slice `slice`: lane column g is
+// the chunk's token g (zeros past its end).
+__device__ __forceinline__ void load_x_block(const MGateUpParams& p, int sc, int nt, int slice, int lane,
+                                             uint32_t (&b)[16][2]) {
   const int g = lane >> 2, t4 = lane & 3;
+  if (g < nt) {
+    const int tok = __ldcg(&p.rt->sc_tok[sc][g]);
+    const uint4* src = reinterpret_cast<const uint4*>(p.xfrag + (size_t)(tok >> 3) * XFRAG_WORDS_M +
+                                                      (size_t)(slice * 32 + 4 * (tok & 7) + t4) * 32);
 #pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-    uint32_t(&b)[16][2] = bb == 0 ? b0 : b1;
-    const int k = 8 * bb + g;
-    if (k < nt) {
-      const int tok = __ldcg(&p.rt->sc_tok[sc][k]);
-      const uint4* src = reinterpret_cast<const uint4*>(p.xfrag + (size_t)(tok >> 3) * XFRAG_WORDS_M +
-                                                        (size_t)(slice * 32 + 4 * (tok & 7) + t4) * 32);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = __ldcg(src + q);
-        b[2 * q][0] = v.x;
-        b[2 * q][1] = v.y;
-        b[2 * q + 1][0] = v.z;
-        b[2 * q + 1][1] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int kb = 0; kb < 16; ++kb) b[kb][0] = b[kb][1] = 0u;
+    for (int q = 0; q < 8; ++q) {
+      const uint4 v = __ldcg(src + q);
+      b[2 * q][0] = v.x;
+      b[2 * q][1] = v.y;
+      b[2 * q + 1][0] = v.z;
+      b[2 * q + 1][1] = v.w;
     }
+  } else {
+#pragma unroll
+    for (int kb = 0; kb < 16; ++kb) b[kb][0] = b[kb][1] = 0u;
   }
 }
 
 __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + (size_t)MG_STAGES * M_TILE);  // [MG_RED][2][8][128]
-  float* ts_s = red + MG_RED * 2 * MG_CW * 128;
+  float* red = reinterpret_cast<float*>(smem + (size_t)MG_STAGES * M_TILE);  // [MG_RED][8][128]
+  float* ts_s = red + MG_RED * MG_CW * 128;
   uint64_t* full = reinterpret_cast<uint64_t*>(ts_s + TS_WORDS);
   uint64_t* empty = full + MG_STAGES;
   uint64_t* rfull = empty + MG_STAGES;
@@ -286,81 +287,49 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
   int lo, hi;
   item_range(n_items, lo, hi);
 
-  if (warp == MG_CW) {
+  if (warp == MG_PW) {
     if (lane == 0) produce_items(p.experts, p.rt, 0, GU_TILES, lo, hi, stages, full, empty, p.err);
     return;
   }
 
-  if (warp < MG_CW) {
-    // ---- compute warps: warp w multiplies K-slice w of every item.  Two
-    // consecutive items of one slot-chunk of at most 8 tokens go through the
-    // interleaved two-slice product (the same bits as two single products).
-    uint32_t b0[16][2], b1[16][2];
+  if (warp < MG_PW) {
+    // ---- compute group grp takes items n = grp (mod MG_GROUPS); its warp kw
+    // multiplies K-slice kw of each.
+    const int grp = warp / MG_CW, kw = warp % MG_CW;
+    uint32_t bfr[16][2];
     int cur = -1, nt = 0;
-    auto hand_over = [&](int n, const float (&a0)[4], const float (&a1)[4]) {
-      const int b = n % MG_RED;
-      if (n >= MG_RED && !mbar_wait(&rempty[b], ((n / MG_RED) - 1) & 1)) atomicOr(p.err, ERR_WAIT_EMPTY);
-      float* rb = red + (size_t)b * 2 * MG_CW * 128;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) rb[warp * 128 + j * 32 + lane] = a0[j];
-      if (nt > 8) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) rb[(MG_CW + warp) * 128 + j * 32 + lane] = a1[j];
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&rfull[b]);
-    };
-    for (int n = 0; lo + n < hi;) {
+    for (int n = grp; lo + n < hi; n += MG_GROUPS) {
       const int i = lo + n, sc = i / GU_TILES, s = n % MG_STAGES;
       if (sc != cur) {
         cur = sc;
         nt = __ldcg(&p.rt->sc_n[sc]);
-        load_x_blocks(p, sc, nt, warp, lane, b0, b1);
+        load_x_block(p, sc, nt, kw, lane, bfr);
       }
-      float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-      if (nt <= 8 && lo + n + 1 < hi && (i + 1) / GU_TILES == sc) {
-        const int s1 = (n + 1) % MG_STAGES;
-        const bool ok = mbar_wait(&full[s], (n / MG_STAGES) & 1) && mbar_wait(&full[s1], ((n + 1) / MG_STAGES) & 1);
-        if (ok)
-          nvfp4_slice_mma2(stages + (size_t)s * M_TILE + warp * F4_SLICE, stages + (size_t)s1 * M_TILE + warp * F4_SLICE,
-                           lane, b0, acc0, acc1);
-        else
-          atomicOr(p.err, ERR_WAIT_FULL);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&empty[s]);
-          mbar_arrive(&empty[s1]);
-        }
-        const float z[4] = {0.f, 0.f, 0.f, 0.f};
-        hand_over(n, acc0, z);
-        hand_over(n + 1, acc1, z);
-        n += 2;
-        continue;
-      }
-      if (mbar_wait(&full[s], (n / MG_STAGES) & 1)) {
-        const uint8_t* sl = stages + (size_t)s * M_TILE + warp * F4_SLICE;
-        if (nt > 8)
-          nvfp4_slice_mma_n16(sl, lane, b0, b1, acc0, acc1);
-        else
-          nvfp4_slice_mma(sl, lane, b0, acc0);
-      } else {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mbar_wait(&full[s], (n / MG_STAGES) & 1))
+        nvfp4_slice_mma(stages + (size_t)s * M_TILE + kw * F4_SLICE, lane, bfr, acc);
+      else
         atomicOr(p.err, ERR_WAIT_FULL);
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      hand_over(n, acc0, acc1);
-      n += 1;
+      const int b = n % MG_RED;
+      if (n >= MG_RED && !mbar_wait(&rempty[b], ((n / MG_RED) - 1) & 1)) atomicOr(p.err, ERR_WAIT_EMPTY);
+      float* rb = red + (size_t)b * MG_CW * 128;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) rb[kw * 128 + j * 32 + lane] = acc[j];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[b]);
     }
     return;
   }
 
   // ---- epilogue warps: warp q takes items n = q (mod MG_EW), whose partial
   // sums arrive in ring buffer q; lane = (token k = 4 h + lane / 8 for
-  // h = 0..3, gate/up row lane % 8 of the tile).
-  const int q = warp - (MG_CW + 1);
+  // h = 0, 1, gate/up row lane % 8 of the tile).
+  const int q = warp - (MG_PW + 1);
   const int ep_tk = lane >> 3, ep_row = lane & 7;
   int cur = -1, nt = 0, pair0 = 0;
-  float fk[4] = {0.f, 0.f, 0.f, 0.f};  // 2^-exponent x gate/up tensor scale of tokens 4 h + ep_tk
+  float fk[2] = {0.f, 0.f};  // 2^-exponent x gate/up tensor scale of tokens 4 h + ep_tk
   for (int n = q; lo + n < hi; n += MG_EW) {
     const int i = lo + n, sc = i / GU_TILES, tile = i % GU_TILES;
     if (sc != cur) {  // before the wait: the table reads overlap the tile's arithmetic
@@ -369,7 +338,7 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
       pair0 = __ldcg(&p.rt->sc_pair[sc]);
       const float ts = ts_s[2 * __ldcg(&p.rt->sc_e[sc])];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
+      for (int h = 0; h < 2; ++h) {
         const int k = 4 * h + ep_tk;
         fk[h] = k < nt ? __fmul_rn(exp2i(-__ldcg(p.xh_exp + __ldcg(&p.rt->sc_tok[sc][k]))), ts) : 0.f;
       }
@@ -378,18 +347,17 @@ __global__ void __launch_bounds__(MG_THREADS, 1) mgateup_kernel(const MGateUpPar
       atomicOr(p.err, ERR_WAIT_FULL);
       break;
     }
-    const float* rb = red + (size_t)q * 2 * MG_CW * 128;
+    const float* rb = red + (size_t)q * MG_CW * 128;
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
+    for (int h = 0; h < 2; ++h) {
       const int k = 4 * h + ep_tk;
       if (k < nt) {
-        const int bb = k >> 3;
-        const int og = red_off(ep_row, k & 7), ou = red_off(ep_row + 8, k & 7);
+        const int og = red_off(ep_row, k), ou = red_off(ep_row + 8, k);
         float gsum = 0.f, usum = 0.f;
 #pragma unroll
         for (int w = 0; w < MG_CW; ++w) {
-          gsum += rb[(bb * MG_CW + w) * 128 + og];
-          usum += rb[(bb * MG_CW + w) * 128 + ou];
+          gsum += rb[w * 128 + og];
+          usum += rb[w * 128 + ou];
         }
         const float gate = __fmul_rn(gsum, fk[h]);
         const float up = __fmul_rn(usum, fk[h]);
@@ -416,62 +384,57 @@ struct MDownParams {
 
 constexpr int MD_BLOCKS = H / 64;  // 64-row items per expert
 
-constexpr int MD_RED_SET = 2 * 4 * 2 * 128;  // floats: [2 items][4 row tiles][2 blocks][128]
+constexpr int MD_RED_SET = 2 * 4 * 128;  // floats: [2 items][4 row tiles][128]
 
 __host__ __device__ constexpr size_t mdown_smem_bytes() {
-  // [stages][red 2 sets][tensor scales][full, empty][hx 4 x 2 x 16]
-  return (size_t)MG_STAGES * M_TILE + 2 * MD_RED_SET * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8 + 4 * 2 * 16 * 4;
+  // [stages][red 2 sets][tensor scales][full, empty][hx 4 x 2 x 8]
+  return (size_t)MG_STAGES * M_TILE + 2 * MD_RED_SET * 4 + TS_WORDS * 4 + 2 * MG_STAGES * 8 + 4 * 2 * 8 * 4;
 }
 
 // h of slot-chunk sc, K half kh, as f16 B fragments scaled by 2^e(pair), e
 // from the pair's largest |h| over both K halves: each warp takes the maximum
 // of its half, and the two warps of row tile rtile swap them through hx
-// ([4 row tiles][2 halves][16 tokens]) on named barrier 1 + rtile.  ex[bb]:
-// the exponent of this lane's token 8 bb + lane / 4.
-__device__ __forceinline__ void load_h_blocks(const MDownParams& p, int pair0, int nt, int rtile, int kh, int lane,
-                                              unsigned* hx, uint32_t (&b0)[16][2], uint32_t (&b1)[16][2],
-                                              int (&ex)[2]) {
+// ([4 row tiles][2 halves][8 tokens]) on named barrier 1 + rtile.  Returns the
+// exponent of this lane's token lane / 4.
+__device__ __forceinline__ int load_h_block(const MDownParams& p, int pair0, int nt, int rtile, int kh, int lane,
+                                            unsigned* hx, uint32_t (&b)[16][2]) {
   const int g = lane >> 2, t4 = lane & 3;
+  uint32_t mx = 0u;  // largest |h| so far, as two bf16 magnitudes
+  if (g < nt) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(p.h + (size_t)(pair0 + g) * I) + kh * 128 + t4;
 #pragma unroll
-  for (int bb = 0; bb < 2; ++bb) {
-    uint32_t(&b)[16][2] = bb == 0 ? b0 : b1;
-    const int k = 8 * bb + g;
-    uint32_t mx = 0u;  // largest |h| so far, as two bf16 magnitudes
-    if (k < nt) {
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.h + (size_t)(pair0 + k) * I) + kh * 128 + t4;
-#pragma unroll
-      for (int kb = 0; kb < 16; ++kb) {
-        b[kb][0] = __ldcg(src + kb * 8);
-        b[kb][1] = __ldcg(src + kb * 8 + 4);
-      }
-#pragma unroll
-      for (int kb = 0; kb < 16; ++kb) {
-        mx = __vmaxu2(mx, b[kb][0] & 0x7FFF7FFFu);
-        mx = __vmaxu2(mx, b[kb][1] & 0x7FFF7FFFu);
-      }
-    } else {
-#pragma unroll
-      for (int kb = 0; kb < 16; ++kb) b[kb][0] = b[kb][1] = 0u;
+    for (int kb = 0; kb < 16; ++kb) {
+      b[kb][0] = __ldcg(src + kb * 8);
+      b[kb][1] = __ldcg(src + kb * 8 + 4);
     }
-    mx = max(mx & 0xFFFFu, mx >> 16);
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (t4 == 0) hx[(rtile * 2 + kh) * 16 + k] = mx;
-    named_bar_sync(1 + rtile, 64);
-    mx = max(mx, hx[(rtile * 2 + (kh ^ 1)) * 16 + k]);
-    // As fp32 bits (<< 16) the order of non-negative values is that of their bits.
-    ex[bb] = f16_range_exp(__uint_as_float(mx << 16));
-    const float sc = exp2i(ex[bb]);
 #pragma unroll
-    for (int kb = 0; kb < 16; ++kb)
+    for (int kb = 0; kb < 16; ++kb) {
+      mx = __vmaxu2(mx, b[kb][0] & 0x7FFF7FFFu);
+      mx = __vmaxu2(mx, b[kb][1] & 0x7FFF7FFFu);
+    }
+  } else {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint32_t v = b[kb][r];
-        const __half2 hv = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), sc),
-                                             __fmul_rn(__uint_as_float(v & 0xFFFF0000u), sc));
-        b[kb][r] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
+    for (int kb = 0; kb < 16; ++kb) b[kb][0] = b[kb][1] = 0u;
   }
+  mx = max(mx & 0xFFFFu, mx >> 16);
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  if (t4 == 0) hx[(rtile * 2 + kh) * 8 + g] = mx;
+  named_bar_sync(1 + rtile, 64);
+  mx = max(mx, hx[(rtile * 2 + (kh ^ 1)) * 8 + g]);
+  // As fp32 bits (<< 16) the order of non-negative values is that of their bits.
+  const int ex = f16_range_exp(__uint_as_float(mx << 16));
+  const float sc = exp2i(ex);
+#pragma unroll
+  for (int kb = 0; kb < 16; ++kb)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const uint32_t v = b[kb][r];
+      const __half2 hv = __floats2half2_rn(__fmul_rn(__uint_as_float(v << 16), sc),
+                                           __fmul_rn(__uint_as_float(v & 0xFFFF0000u), sc));
+      b[kb][r] = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+  return ex;
 }
 
 // Warp w: row tile rt = w / 2 of the item's 64 rows, K half kh = w % 2.  The
@@ -511,46 +474,39 @@ __global__ void __launch_bounds__(MD_THREADS, 1) mdown_kernel(const MDownParams 
 
   const int rtile = warp >> 1, kh = warp & 1;
   const int g = lane >> 2, t4 = lane & 3;
-  uint32_t b0[16][2], b1[16][2];
+  uint32_t b0[16][2];
   int cur = -1, nt = 0, pair0 = 0;
-  float fsc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // 2^-e of this lane's output columns
+  float fsc[2] = {0.f, 0.f};  // tensor scale x 2^-e of this lane's output columns 2 t4 + j
   for (int n = 0, u = 0; lo + n < hi;) {
     const int i = lo + n, sc = i / MD_BLOCKS, blk = i % MD_BLOCKS, s = n % MG_STAGES;
     if (sc != cur) {
       cur = sc;
       nt = __ldcg(&p.rt->sc_n[sc]);
       pair0 = __ldcg(&p.rt->sc_pair[sc]);
-      int ex[2];
-      load_h_blocks(p, pair0, nt, rtile, kh, lane, hx, b0, b1, ex);
+      const int ex = load_h_block(p, pair0, nt, rtile, kh, lane, hx, b0);
       const float ts = ts_s[2 * __ldcg(&p.rt->sc_e[sc]) + 1];
 #pragma unroll
-      for (int bb = 0; bb < 2; ++bb)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int k = 8 * bb + 2 * t4 + j;  // output column: token of lanes 4 (2 t4 + j) ..
-          const int e = __shfl_sync(0xffffffffu, ex[bb], (2 * t4 + j) * 4);
-          fsc[bb][j] = k < nt ? __fmul_rn(ts, exp2i(-e)) : 0.f;
-        }
+      for (int j = 0; j < 2; ++j) {
+        const int k = 2 * t4 + j;  // output column: the token of lanes 4 k ..
+        const int e = __shfl_sync(0xffffffffu, ex, k * 4);
+        fsc[j] = k < nt ? __fmul_rn(ts, exp2i(-e)) : 0.f;
+      }
     }
     // One exchange between the two warps of the row tile: one item, or two
-    // consecutive items of a slot-chunk of at most 8 tokens through the
-    // interleaved two-slice product.  Exchange u uses buffer set u & 1.
-    const bool two = nt <= 8 && lo + n + 1 < hi && (i + 1) / MD_BLOCKS == sc;
+    // consecutive items of the slot-chunk through the interleaved two-slice
+    // product.  Exchange u uses buffer set u & 1.
+    const bool two = lo + n + 1 < hi && (i + 1) / MD_BLOCKS == sc;
     const int s1 = (n + 1) % MG_STAGES;
     const int sl_off = (rtile * 2 + kh) * F4_SLICE;
-    float acc[2][2][4] = {};  // [item][block][4]
+    float acc[2][4] = {};  // [item][4]
     if (two) {
       if (mbar_wait(&full[s], (n / MG_STAGES) & 1) && mbar_wait(&full[s1], ((n + 1) / MG_STAGES) & 1))
         nvfp4_slice_mma2(stages + (size_t)s * M_TILE + sl_off, stages + (size_t)s1 * M_TILE + sl_off, lane, b0,
-                         acc[0][0], acc[1][0]);
+                         acc[0], acc[1]);
       else
         atomicOr(p.err, ERR_WAIT_FULL);
     } else if (mbar_wait(&full[s], (n / MG_STAGES) & 1)) {
-      const uint8_t* sl = stages + (size_t)s * M_TILE + sl_off;
-      if (nt > 8)
-        nvfp4_slice_mma_n16(sl, lane, b0, b1, acc[0][0], acc[0][1]);
-      else
-        nvfp4_slice_mma(sl, lane, b0, acc[0][0]);
+      nvfp4_slice_mma(stages + (size_t)s * M_TILE + sl_off, lane, b0, acc[0]);
     } else {
       atomicOr(p.err, ERR_WAIT_FULL);
     }
@@ -560,31 +516,25 @@ __global__ void __launch_bounds__(MD_THREADS, 1) mdown_kernel(const MDownParams 
       if (two) mbar_arrive(&empty[s1]);
     }
     const int items = two ? 2 : 1;
-    float* rset = red + (size_t)(u & 1) * MD_RED_SET;  // [2 items][4 row tiles][2 blocks][128]
+    float* rset = red + (size_t)(u & 1) * MD_RED_SET;  // [2 items][4 row tiles][128]
     if (kh == 1) {
       for (int it = 0; it < items; ++it)
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb)
-          *reinterpret_cast<float4*>(rset + ((it * 4 + rtile) * 2 + bb) * 128 + lane * 4) =
-              make_float4(acc[it][bb][0], acc[it][bb][1], acc[it][bb][2], acc[it][bb][3]);
+        *reinterpret_cast<float4*>(rset + (it * 4 + rtile) * 128 + lane * 4) =
+            make_float4(acc[it][0], acc[it][1], acc[it][2], acc[it][3]);
     }
     named_bar_sync(1 + rtile, 64);
     if (kh == 0) {
       for (int it = 0; it < items; ++it) {
         const int row = (blk + it) * 64 + rtile * 16 + g;
+        const float4 o = *reinterpret_cast<const float4*>(rset + (it * 4 + rtile) * 128 + lane * 4);
+        const float v[4] = {acc[it][0] + o.x, acc[it][1] + o.y, acc[it][2] + o.z, acc[it][3] + o.w};
 #pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const float4 o = *reinterpret_cast<const float4*>(rset + ((it * 4 + rtile) * 2 + bb) * 128 + lane * 4);
-          const float v[4] = {acc[it][bb][0] + o.x, acc[it][bb][1] + o.y, acc[it][bb][2] + o.z,
-                              acc[it][bb][3] + o.w};
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int k = 8 * bb + 2 * t4 + j;
-            if (k < nt) {
-              float* dst = p.part + (size_t)(pair0 + k) * H + row;
-              dst[0] = __fmul_rn(v[j], fsc[bb][j]);
-              dst[8] = __fmul_rn(v[2 + j], fsc[bb][j]);
-            }
+        for (int j = 0; j < 2; ++j) {
+          const int k = 2 * t4 + j;
+          if (k < nt) {
+            float* dst = p.part + (size_t)(pair0 + k) * H + row;
+            dst[0] = __fmul_rn(v[j], fsc[j]);
+            dst[8] = __fmul_rn(v[2 + j], fsc[j]);
           }
         }
       }

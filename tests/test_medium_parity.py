@@ -2,9 +2,9 @@
 
 Same entry points as the decode path (flint_moe_decode_layer / _stack); past 8
 tokens they run the expert-grouped kernels.  Full-size shapes; the batches
-cover one partial chunk of 8 (9, 17, 40), whole chunks (16, 32, 64), experts
-chosen by more than 16 tokens (several slot-chunks of one expert) and the
-shared expert's 4 slot-chunks at 64 tokens.
+cover one partial chunk of 8 (9, 17), whole chunks (16, 32, 40, 64), experts
+chosen by more than 8 tokens (several slot-chunks of one expert) and the
+shared expert's 8 slot-chunks at 64 tokens.
 """
 
 import numpy as np
@@ -89,7 +89,7 @@ def test_medium_is_deterministic(layer_cfg0, dev, ws):
 
 def test_medium_experts_shared_by_many_tokens(layer_cfg0, dev, ws):
     """20 copies of one token plus 21 others: the copies' 6 experts each serve
-    at least 20 tokens (two slot-chunks of one expert, 16 + the rest)."""
+    at least 20 tokens (three slot-chunks of one expert: 8, 8 and the rest)."""
     _, lw, L = layer_cfg0
     x = torch.cat([synth.gen_x(0, 1, index=8).repeat(20, 1), synth.gen_x(0, 21, index=9)])
     y, ids, w = run_layer(L, x, dev, ws)
@@ -101,8 +101,8 @@ def test_medium_experts_shared_by_many_tokens(layer_cfg0, dev, ws):
 
 
 def test_medium_all_tokens_identical(layer_cfg0, dev, ws):
-    """64 identical tokens: 6 routed experts with 64 tokens each (4 slot-chunks
-    apiece) and the shared expert's 4."""
+    """64 identical tokens: 6 routed experts with 64 tokens each (8 slot-chunks
+    apiece) and the shared expert's 8."""
     _, lw, L = layer_cfg0
     x = synth.gen_x(0, 1, index=10).repeat(64, 1)
     y, ids, w = run_layer(L, x, dev, ws)
