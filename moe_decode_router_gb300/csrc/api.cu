@@ -304,7 +304,7 @@ int flint_moe_decode_layer(const flint_moe_dims* dims, const flint_moe_layer* la
   DeviceState* ds = nullptr;
   if ((st = device_state(&ds)) != FLINT_MOE_OK) return st;
   if (medium)
-    return to_status(launch_medium_chain(layer_args(*layer), x, B, dims->rms_eps, y, topk_ids, topk_w,
+    return to_status(launch_medium_chain(layer_args(*layer), x, nullptr, B, dims->rms_eps, y, topk_ids, topk_w,
                                          carve_medium_ws(ws), ds->gu_grid, ds->err,
                                          reinterpret_cast<cudaStream_t>(stream), true));
   return launch_one_layer(dims, *layer, x, B, y, topk_ids, topk_w, ws, ds->gu_grid, ds->fused_grid, ds->err,
@@ -386,19 +386,19 @@ int flint_moe_decode_stack(const flint_moe_dims* dims, const flint_moe_layer* la
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e != cudaSuccess) return FLINT_MOE_ERR_CUDA;
   cudaError_t le = cudaSuccess;
-  const void* prev = x;
   for (int i = 0; i < n_layers && le == cudaSuccess && medium; ++i) {
-    // Each sublayer's router computes its own RMSNorm statistics.  A
-    // sublayer's input is read before its output is written, so y_mid can be
-    // both.
+    // The first sublayer normalises x itself; every other one finds its
+    // x_hat in the workspace, left there by the previous sublayer's combine
+    // from its output.
     const bool last = i == n_layers - 1;
     void* ys = ys_per_layer ? static_cast<uint8_t*>(ys_per_layer) + (size_t)i * B * H * 2 : nullptr;
     int32_t* ids = ids_per_layer ? ids_per_layer + (size_t)i * B * TOPK : nullptr;
     float* wl = w_per_layer ? w_per_layer + (size_t)i * B * TOPK : nullptr;
     void* yout = last ? y : (ys ? ys : mw.y_mid);
-    le = launch_medium_chain(layer_args(layers[i]), prev, B, dims->rms_eps, yout, ids, wl, mw, ds->gu_grid, ds->err,
-                             cs, true);
-    prev = yout;
+    LayerArgs nxt{};
+    if (!last) nxt = layer_args(layers[i + 1]);
+    le = launch_medium_chain(layer_args(layers[i]), i == 0 ? x : nullptr, last ? nullptr : &nxt, B, dims->rms_eps,
+                             yout, ids, wl, mw, ds->gu_grid, ds->err, cs, true);
     if (le == cudaSuccess && last && ys) le = cudaMemcpyAsync(ys, y, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, cs);
   }
   for (int i = 0; i < n_layers && le == cudaSuccess && !medium; ++i) {

@@ -46,7 +46,6 @@ struct RouterParams {
   const __nv_bfloat16* wr;      // [E][H]
   float eps;
   int want_f16;
-  int T;                   // tokens of the call; CTA row y handles tokens 8y .. 8y + NB - 1
   __nv_bfloat16* logits;   // [B][E]
   __nv_bfloat16* xh_bf16;  // [B][H] natural layout
   uint32_t* xfrag_f16;     // x_hat * 2^xh_exp[token] in f16, fragment order
@@ -61,17 +60,7 @@ struct RouterParams {
 // owns expert e; thread k owns columns [8k, 8k+8); token pairs share packed
 // fp32x2 arithmetic.
 template <int NB, int EPC>
-__global__ void __launch_bounds__(256, 2) router_kernel(RouterParams p) {
-  // Token chunk of this CTA row (one chunk on the decode path).  Its nb tokens
-  // are rows 8 ch .. 8 ch + nb - 1 of the call; missing rows count as zeros.
-  const int ch = blockIdx.y;
-  const int nb = min(NB, p.T - 8 * ch);
-  p.x += (size_t)ch * 8 * H;
-  p.logits += (size_t)ch * 8 * E;
-  p.xh_bf16 += (size_t)ch * 8 * H;
-  p.xfrag_f16 += (size_t)ch * XFRAG_WORDS;
-  p.xfrag_bf16 += (size_t)ch * XFRAG_WORDS;
-  p.xh_exp += ch * 8;
+__global__ void __launch_bounds__(256, 2) router_kernel(const RouterParams p) {
   constexpr int NP = (NB + 1) / 2;
   constexpr int VP = Pow2Ceil<NB * EPC>::value;
   constexpr int SH = 5 - Log2<VP>::value;
@@ -98,8 +87,7 @@ __global__ void __launch_bounds__(256, 2) router_kernel(RouterParams p) {
   // Issue every dependent load before using any of them (one round trip).
   uint4 xraw[NB];
 #pragma unroll
-  for (int t = 0; t < NB; ++t)
-    xraw[t] = t < nb ? __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H + k0)) : make_uint4(0u, 0u, 0u, 0u);
+  for (int t = 0; t < NB; ++t) xraw[t] = __ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H + k0));
   const bool ss_given = has_norm && p.ss_in != nullptr;
   CSum ssp[DN_TILES / 32];
   if (ss_given && warp < NB) {
@@ -210,7 +198,7 @@ __global__ void __launch_bounds__(256, 2) router_kernel(RouterParams p) {
     if ((lane & ((1 << SH) - 1)) == 0) red[warp][lane >> SH] = tot;
   }
   __syncthreads();
-  if (tid < NB * EPC && tid % NB < nb) {
+  if (tid < NB * EPC) {
     CSum a = red[0][tid];
 #pragma unroll
     for (int w = 1; w < 8; ++w) cs_merge(a, red[w][tid]);
@@ -224,7 +212,6 @@ __global__ void __launch_bounds__(256, 2) router_kernel(RouterParams p) {
     const int ws = k0 >> 8, kb = (k0 & 255) >> 4, rr = (k0 >> 3) & 1;
 #pragma unroll
     for (int t = 0; t < NB; ++t) {
-      if (t >= nb) break;
       uint32_t pk[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -245,7 +232,6 @@ __global__ void __launch_bounds__(256, 2) router_kernel(RouterParams p) {
       __syncthreads();
 #pragma unroll
       for (int t = 0; t < NB; ++t) {
-        if (t >= nb) break;
         const int ex = f16_range_exp(__uint_as_float(xmax[t]));
         const float sc = exp2i(ex);
 #pragma unroll
@@ -870,35 +856,6 @@ static cudaError_t router_carveout() {
                               cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
-cudaError_t launch_router_chunks(const LayerArgs& L, const void* x, int T, float eps, const MediumWs& ws,
-                                 cudaStream_t st, bool pdl) {
-  RouterParams rp;
-  rp.x = static_cast<const __nv_bfloat16*>(x);
-  rp.ss_in = nullptr;
-  rp.norm_w = static_cast<const __nv_bfloat16*>(L.norm_w);
-  rp.wr = static_cast<const __nv_bfloat16*>(L.router_w);
-  rp.eps = eps;
-  rp.want_f16 = 1;
-  rp.T = T;
-  rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
-  rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
-  rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);
-  rp.xfrag_bf16 = static_cast<uint32_t*>(ws.xfrag_bf16);
-  rp.xh_exp = ws.xh_exp;
-  constexpr int EPC = RouterEpc<8>::value;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(E / EPC, (T + 7) / 8);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, router_kernel<8, EPC>, rp);
-}
-
 static cudaError_t launch_router(int B, const RouterParams& rp, cudaStream_t st, bool pdl) {
   switch (B) {
     case 1: return launch_router_nb<1>(rp, st, pdl);
@@ -954,7 +911,6 @@ cudaError_t launch_decode_chain(int fmt, const LayerArgs& L, const void* x, cons
   rp.wr = static_cast<const __nv_bfloat16*>(L.router_w);
   rp.eps = eps;
   rp.want_f16 = fmt == 0;
-  rp.T = B;
   rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
   rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
   rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);

@@ -119,9 +119,8 @@ struct MedRoute {
 };
 struct MediumWs {
   void* logits;      // bf16 [64][256]
-  void* xh_bf16;     // bf16 [64][2048]
+  void* xh_bf16;     // bf16 [64][2048] x_hat
   void* xfrag_f16;   // [8 chunks][8 K-slices][32 lanes][32 words]
-  void* xfrag_bf16;  // same layout, bf16 (written by the router, unused here)
   int* xh_exp;       // [64]
   MedRoute* rt;
   void* h;           // bf16 [MPAIRS][512]
@@ -130,19 +129,19 @@ struct MediumWs {
 };
 constexpr size_t medium_ws_bytes() {
   return ws_align256((size_t)MT_MAX * E * 2) + ws_align256((size_t)MT_MAX * H * 2) +
-         2 * ws_align256((size_t)(MT_MAX / 8) * 8 * 32 * 32 * 4) + ws_align256(MT_MAX * 4) +
+         ws_align256((size_t)(MT_MAX / 8) * 8 * 32 * 32 * 4) + ws_align256(MT_MAX * 4) +
          ws_align256(sizeof(MedRoute)) + ws_align256((size_t)MPAIRS * I * 2) +
          ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2);
 }
 MediumWs carve_medium_ws(void* ws);
 cudaError_t medium_kernels_init();
-// Router over T <= 64 tokens in chunks of 8 (decode.cu).
-cudaError_t launch_router_chunks(const LayerArgs& L, const void* x, int T, float eps, const MediumWs& ws,
-                                 cudaStream_t st, bool pdl);
-// Enqueues one medium sublayer: router, routing tables, gate/up, down, combine.
-cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
-                                float* w_out, const MediumWs& ws, int sm_count, unsigned* err, cudaStream_t st,
-                                bool pdl_first);
+// Enqueues one medium sublayer.  x: the sublayer's input, normalised first
+// (mnorm); null when the previous sublayer's combine already left this
+// sublayer's x_hat in the workspace.  next: non-null when the combine is to
+// leave x_hat for that sublayer (its norm weight, the same eps).
+cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, const LayerArgs* next, int T, float eps, void* y,
+                                int32_t* ids_out, float* w_out, const MediumWs& ws, int sm_count, unsigned* err,
+                                cudaStream_t st, bool pdl_first);
 
 // Small-batch dense GEMV on packed NVFP4 weights (dense.cu): B * K at most
 // DENSE_MAX_BK (the activations are staged in shared memory).

@@ -7,12 +7,15 @@
 // most experts several times (649 MB instead of 355 MB per sublayer at 64
 // tokens).  This path reads every selected expert's weights once per
 // slot-chunk: the tokens of one expert, up to 8 at a time, ride as the mma n8
-// block on each dequantised weight fragment.  Five kernels, chained with
+// block on each dequantised weight fragment.  Kernels, chained with
 // programmatic dependent launch:
 //
-//   router_kernel   (decode.cu) over chunks of 8 tokens: RMSNorm, bf16
-//                   logits (error-free accumulation), x_hat fragments in f16
-//                   scaled by a per-token power of two.
+//   mnorm_kernel    one CTA per token: RMSNorm, x_hat in bf16 and in f16
+//                   scaled by a per-token power of two (first sublayer of a
+//                   call only; inside a stack the previous sublayer's combine
+//                   does this step for the next one).
+//   mlogits_kernel  bf16 router logits (error-free accumulation) over units
+//                   (chunk of 8 tokens, expert), one wave of CTAs.
 //   mroute_kernel   one CTA: sigmoid top-6 per token, then the slot-chunk
 //                   table (expert, up to 8 tokens, first pair) with the
 //                   shared expert first and the routed experts in ascending
@@ -26,7 +29,11 @@
 //                   per-pair power of two (from the pair's largest |h|, which
 //                   the two K-half warps of a row tile find together); writes
 //                   the pair's down projection times its tensor scale, fp32.
-//   mcombine_kernel y = bf16(sum_j w_j d_j + d_shared), j in selection order.
+//   mcombine_kernel one CTA per token: y = bf16(sum_j w_j d_j + d_shared), j
+//                   in selection order; inside a stack also the next
+//                   sublayer's x_hat from y.
+#include <algorithm>
+
 #include "decode_common.cuh"
 #include "flint_internal.h"
 
@@ -35,6 +42,189 @@ namespace flint {
 namespace {
 
 constexpr int XFRAG_WORDS_M = 8 * 32 * 32;  // one chunk of 8 tokens (router fragment layout)
+
+// ------------------------------------------------------------------ common item walk
+
+// Items [lo, hi) of this CTA: a contiguous range, so that consecutive items
+// mostly share a slot-chunk.
+__device__ __forceinline__ void item_range(int n_items, int& lo, int& hi) {
+  const int G = gridDim.x;
+  const int q = (n_items + G - 1) / G;
+  lo = min(n_items, (int)blockIdx.x * q);
+  hi = min(n_items, lo + q);
+}
+
+// ------------------------------------------------------------------ x_hat
+
+// Where x_hat goes: bf16 in the natural layout (the logits read it), f16
+// times 2^xh_exp[t] in the mma fragment order of its chunk of 8 tokens (the
+// gate/up kernel reads it), and the exponent itself.
+struct XhatOut {
+  __nv_bfloat16* xh;  // [T][H]
+  uint32_t* xfrag;    // [chunks][XFRAG_WORDS_M]
+  int* xh_exp;        // [T]
+};
+
+// x_hat of token t by a CTA of 256 threads; thread k holds columns 8k..8k+7
+// of the token's input (bf16 values as fp32) in v.  With a norm weight
+// (RMSNorm, "Day-0 Support for Flint on vLLM", section "Model architecture"):
+// r = 1 / sqrt(sum(x^2) / H + eps) from a compensated sum of squares, so r is
+// the one the exact sum gives whatever the order; x_hat = bf16(x * r * w).
+// Without one, x_hat = x.  xh_exp[t] puts max |x_hat| into [2^14, 2^15).
+__device__ __forceinline__ void publish_xhat(float (&v)[8], bool has_norm, const float (&nw)[8], float eps, int t,
+                                             const XhatOut& o) {
+  __shared__ CSum s_ss[8];
+  __shared__ unsigned s_mx[8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, k0 = tid * 8;
+  if (has_norm) {
+    CSum2 a2 = {0ull, 0ull};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t q = f2pack(v[2 * i], v[2 * i + 1]);
+      cs2_add(a2, f2mul(q, q));
+    }
+    CSum a, b;
+    cs2_split(a2, a, b);
+    cs_merge(a, b);
+    a = cs_warp_reduce(a);
+    if (lane == 0) s_ss[warp] = a;
+    __syncthreads();
+    a = s_ss[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) cs_merge(a, s_ss[w]);
+    const float ms = __fmul_rn(cs_value(a), 1.0f / (float)H);
+    const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(v[i], r), nw[i])));
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  const unsigned wm = redux_max(__float_as_uint(m));
+  if (lane == 0) s_mx[warp] = wm;
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pk[i] = (__float_as_uint(v[2 * i]) >> 16) | (__float_as_uint(v[2 * i + 1]) & 0xFFFF0000u);
+  *reinterpret_cast<uint4*>(o.xh + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  __syncthreads();
+  unsigned mx = s_mx[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) mx = max(mx, s_mx[w]);
+  const int ex = f16_range_exp(__uint_as_float(mx));
+  const float sc = exp2i(ex);
+  // Columns 8k..8k+7: K-slice k / 32, block (k % 32) / 2, register k % 2 of
+  // the lanes 4 (t % 8) .. 4 (t % 8) + 3.
+  const int ws = k0 >> 8, kb = (k0 & 255) >> 4, rr = (k0 >> 3) & 1;
+  uint32_t* fr = o.xfrag + (size_t)(t >> 3) * XFRAG_WORDS_M;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 hv = __floats2half2_rn(__fmul_rn(v[2 * i], sc), __fmul_rn(v[2 * i + 1], sc));
+    fr[((ws * 32 + 4 * (t & 7) + i) * 16 + kb) * 2 + rr] = *reinterpret_cast<const uint32_t*>(&hv);
+  }
+  if (tid == 0) o.xh_exp[t] = ex;
+}
+
+struct MNormParams {
+  const __nv_bfloat16* x;       // [T][H]
+  const __nv_bfloat16* norm_w;  // [H] or null
+  float eps;
+  XhatOut o;
+};
+
+__global__ void __launch_bounds__(256) mnorm_kernel(const MNormParams p) {
+  const int t = blockIdx.x, k0 = threadIdx.x * 8;
+  const bool has_norm = p.norm_w != nullptr;
+  float nw[8] = {};
+  if (has_norm) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.norm_w + k0)), nw);
+  pdl_trigger();
+  pdl_wait();
+  float v[8];
+  bf16x8_to_f32(__ldcg(reinterpret_cast<const uint4*>(p.x + (size_t)t * H + k0)), v);
+  publish_xhat(v, has_norm, nw, p.eps, t, p.o);
+}
+
+// ------------------------------------------------------------------ logits
+
+// logit[t][e] = bf16(sum_k x_hat[t][k] W_r[e][k]), accumulated error-free
+// (bf16 products are exact in fp32, TwoSum carries every rounding error), so
+// it is the correctly rounded value whatever the order.  Units u = (chunk c =
+// u / E, expert e = u % E); each CTA takes a contiguous range of units, so it
+// keeps a chunk's 8 rows of x_hat in registers over many experts and reads
+// one 4 KB router row per unit.  Thread k owns columns 8k..8k+7; token pairs
+// share packed fp32x2 arithmetic.
+struct MLogitsParams {
+  const __nv_bfloat16* wr;  // [E][H]
+  const __nv_bfloat16* xh;  // [T][H]
+  int T;
+  __nv_bfloat16* logits;    // [T][E]
+};
+
+__device__ __forceinline__ void load_xhat_chunk(const MLogitsParams& p, int c, int k0, uint4 (&xr)[8]) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    xr[t] = 8 * c + t < p.T ? __ldcg(reinterpret_cast<const uint4*>(p.xh + (size_t)(8 * c + t) * H + k0))
+                            : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__global__ void __launch_bounds__(256, 2) mlogits_kernel(const MLogitsParams p) {
+  __shared__ CSum red[2][8][8];  // [unit parity][warp][token]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, k0 = tid * 8;
+  const int NC = (p.T + 7) >> 3;
+  int lo, hi;
+  item_range(E * NC, lo, hi);
+  // Router rows are constants: ask this CTA's rows into L2 before the wait.
+  if (tid == 0)
+    for (int u = lo; u < hi; ++u) bulk_prefetch_l2(p.wr + (size_t)(u % E) * H, H * 2);
+  uint4 wnext = lo < hi ? __ldg(reinterpret_cast<const uint4*>(p.wr + (size_t)(lo % E) * H + k0)) : make_uint4(0u, 0u, 0u, 0u);
+  pdl_trigger();
+  pdl_wait();
+  if (lo >= hi) return;
+  uint4 xa[8], xb[8];
+  int ca = lo / E;
+  const int c_last = (hi - 1) / E;
+  load_xhat_chunk(p, ca, k0, xa);
+  if (ca + 1 <= c_last) load_xhat_chunk(p, ca + 1, k0, xb);
+  for (int u = lo; u < hi; ++u) {
+    const int c = u / E, e = u % E;
+    if (c != ca) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) xa[t] = xb[t];
+      ca = c;
+      if (ca + 1 <= c_last) load_xhat_chunk(p, ca + 1, k0, xb);
+    }
+    const uint4 wcur = wnext;
+    if (u + 1 < hi) wnext = __ldg(reinterpret_cast<const uint4*>(p.wr + (size_t)((u + 1) % E) * H + k0));
+    float wf[8];
+    bf16x8_to_f32(wcur, wf);
+    CSum2 d2[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d2[q] = CSum2{0ull, 0ull};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint64_t w2 = f2pack(wf[i], wf[i]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t a = (&xa[2 * q].x)[i >> 1], b = (&xa[2 * q + 1].x)[i >> 1];
+        const float x0 = __uint_as_float((i & 1) ? (a & 0xFFFF0000u) : (a << 16));
+        const float x1 = __uint_as_float((i & 1) ? (b & 0xFFFF0000u) : (b << 16));
+        cs2_add(d2[q], f2mul(f2pack(x0, x1), w2));
+      }
+    }
+    CSum d[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cs2_split(d2[q], d[2 * q], d[2 * q + 1]);
+    const CSum tot = cs_reduce_scatter<8>(d, lane);  // lanes 4t..4t+3: token t
+    CSum(*rb)[8] = red[(u - lo) & 1];
+    if ((lane & 3) == 0) rb[warp][lane >> 2] = tot;
+    __syncthreads();
+    if (tid < 8 && 8 * c + tid < p.T) {
+      CSum a = rb[0][tid];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) cs_merge(a, rb[w][tid]);
+      p.logits[(size_t)(8 * c + tid) * E + e] = __float2bfloat16_rn(cs_value(a));
+    }
+  }
+}
 
 // ------------------------------------------------------------------ routing tables
 
@@ -68,12 +258,19 @@ __global__ void __launch_bounds__(MR_THREADS, 1) mroute_kernel(const MRouteParam
     s_cnt[E] = (unsigned)T;
     s_mask[E] = T == 64 ? ~0ull : ((1ull << T) - 1ull);
   }
-  // Top-6 of token t by warp t % 32.
-  for (int t = warp; t < T; t += 32) {
-    const uint4 raw = load_logits(p.logits + (size_t)t * E, lane);
+  // Top-6 of tokens warp and warp + 32; both logits rows are requested first.
+  static_assert(MT_MAX <= 64, "two tokens per warp");
+  uint4 raw[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (warp + 32 * h < T) raw[h] = load_logits(p.logits + (size_t)(warp + 32 * h) * E, lane);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = warp + 32 * h;
+    if (t >= T) break;
     int sel_i[TOPK];
     uint32_t sel_lg[TOPK];
-    warp_top6_core(raw, lane, sel_i, sel_lg);
+    warp_top6_core(raw[h], lane, sel_i, sel_lg);
     warp_top6_weights(sel_lg, lane, s_w[t]);
     if (lane < TOPK) {
       int wi = 0;
@@ -128,30 +325,23 @@ __global__ void __launch_bounds__(MR_THREADS, 1) mroute_kernel(const MRouteParam
     }
   }
   __syncthreads();
-  // Slot-chunks of expert e, tokens in ascending order.
-  if (tid < NE) {
-    const int e = tid, n = (int)s_cnt[e];
-    if (n > 0) {
-      const int c0 = s_cbase[e], pb = s_pbase[e];
-      for (int c = 0; c * MCH < n; ++c) {
-        p.rt->sc_e[c0 + c] = e;
-        p.rt->sc_pair[c0 + c] = pb + c * MCH;
-        p.rt->sc_n[c0 + c] = min(MCH, n - c * MCH);
-      }
-      unsigned long long m = s_mask[e];
-      for (int k = 0; m != 0ull; ++k) {
-        const int t = __ffsll((long long)m) - 1;
-        m &= m - 1ull;
-        p.rt->sc_tok[c0 + k / MCH][k % MCH] = (uint8_t)t;
-      }
-    }
-  }
-  // Pair of (token t, selection j): the expert's base + the tokens before t.
+  // Every (token t, selection j) in one pass: its rank among the expert's
+  // tokens (ascending) gives its pair, its slot-chunk and its place there; the
+  // first token of a slot-chunk also writes the slot-chunk's entry.
   for (int q = tid; q < T * (TOPK + 1); q += MR_THREADS) {
     const int t = q / (TOPK + 1), j = q % (TOPK + 1);
     const int e = j < TOPK ? s_ids[t][j] : E;
     const unsigned long long before = t == 0 ? 0ull : (s_mask[e] & ((1ull << t) - 1ull));
-    p.rt->pidx[t][j] = s_pbase[e] + __popcll(before);
+    const int rank = __popcll(before);
+    const int pr = s_pbase[e] + rank;
+    const int c = s_cbase[e] + rank / MCH;
+    p.rt->pidx[t][j] = pr;
+    p.rt->sc_tok[c][rank % MCH] = (uint8_t)t;
+    if (rank % MCH == 0) {
+      p.rt->sc_e[c] = e;
+      p.rt->sc_pair[c] = pr;
+      p.rt->sc_n[c] = min(MCH, (int)s_cnt[e] - rank);
+    }
   }
   for (int q = tid; q < T * TOPK; q += MR_THREADS) {
     const int t = q / TOPK, j = q % TOPK;
@@ -159,17 +349,6 @@ __global__ void __launch_bounds__(MR_THREADS, 1) mroute_kernel(const MRouteParam
     if (p.ids_out) p.ids_out[q] = s_ids[t][j];
     if (p.w_out) p.w_out[q] = s_w[t][j];
   }
-}
-
-// ------------------------------------------------------------------ common item walk
-
-// Items [lo, hi) of this CTA: a contiguous range, so that consecutive items
-// mostly share a slot-chunk.
-__device__ __forceinline__ void item_range(int n_items, int& lo, int& hi) {
-  const int G = gridDim.x;
-  const int q = (n_items + G - 1) / G;
-  lo = min(n_items, (int)blockIdx.x * q);
-  hi = min(n_items, lo + q);
 }
 
 constexpr int M_TILE = 18432;  // one item's weights: 16 gate/up rows or 64 down rows, all of K
@@ -549,33 +728,46 @@ __global__ void __launch_bounds__(MD_THREADS, 1) mdown_kernel(const MDownParams 
 struct MCombineParams {
   const MedRoute* rt;
   const float* part;
-  int T;
-  __nv_bfloat16* y;  // [T][H]
+  __nv_bfloat16* y;                  // [T][H]
+  int publish;                       // also x_hat of the next sublayer from y
+  const __nv_bfloat16* next_norm_w;  // its norm weight, or null
+  float eps;
+  XhatOut o;
 };
 
+// One CTA per token t; thread k covers columns 8k..8k+7.
 __global__ void __launch_bounds__(256) mcombine_kernel(const MCombineParams p) {
+  const int t = blockIdx.x, k0 = threadIdx.x * 8;
+  const bool has_norm = p.publish && p.next_norm_w != nullptr;
+  float nw[8] = {};
+  if (has_norm) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.next_norm_w + k0)), nw);
   pdl_wait();
   pdl_trigger();
-  const int q = blockIdx.x * 256 + threadIdx.x;  // (token, 4 columns)
-  if (q >= p.T * (H / 4)) return;
-  const int t = q / (H / 4), c = (q % (H / 4)) * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float acc[8] = {};
 #pragma unroll
   for (int j = 0; j < TOPK; ++j) {
     const float w = __ldcg(&p.rt->w[t][j]);
-    const float4 d = __ldcg(reinterpret_cast<const float4*>(p.part + (size_t)__ldcg(&p.rt->pidx[t][j]) * H + c));
-    acc.x = __fmaf_rn(w, d.x, acc.x);
-    acc.y = __fmaf_rn(w, d.y, acc.y);
-    acc.z = __fmaf_rn(w, d.z, acc.z);
-    acc.w = __fmaf_rn(w, d.w, acc.w);
+    const float4* d = reinterpret_cast<const float4*>(p.part + (size_t)__ldcg(&p.rt->pidx[t][j]) * H + k0);
+    const float4 d0 = __ldcg(d), d1 = __ldcg(d + 1);
+    const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = __fmaf_rn(w, dv[i], acc[i]);
   }
-  const float4 d = __ldcg(reinterpret_cast<const float4*>(p.part + (size_t)__ldcg(&p.rt->pidx[t][TOPK]) * H + c));
-  const __nv_bfloat162 lo = __floats2bfloat162_rn(__fadd_rn(acc.x, d.x), __fadd_rn(acc.y, d.y));
-  const __nv_bfloat162 hi = __floats2bfloat162_rn(__fadd_rn(acc.z, d.z), __fadd_rn(acc.w, d.w));
-  uint2 o;
-  o.x = *reinterpret_cast<const uint32_t*>(&lo);
-  o.y = *reinterpret_cast<const uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p.y + (size_t)t * H + c) = o;
+  const float4* ds = reinterpret_cast<const float4*>(p.part + (size_t)__ldcg(&p.rt->pidx[t][TOPK]) * H + k0);
+  const float4 s0 = __ldcg(ds), s1 = __ldcg(ds + 1);
+  const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  float v[8];
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b2 =
+        __floats2bfloat162_rn(__fadd_rn(acc[2 * i], sv[2 * i]), __fadd_rn(acc[2 * i + 1], sv[2 * i + 1]));
+    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    v[2 * i] = __low2float(b2);
+    v[2 * i + 1] = __high2float(b2);
+  }
+  *reinterpret_cast<uint4*>(p.y + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  if (p.publish) publish_xhat(v, has_norm, nw, p.eps, t, p.o);
 }
 
 template <typename... KArgs, typename... Args>
@@ -605,8 +797,6 @@ MediumWs carve_medium_ws(void* ws) {
   q += ws_align256((size_t)MT_MAX * H * 2);
   w.xfrag_f16 = q;
   q += ws_align256((size_t)(MT_MAX / 8) * XFRAG_WORDS_M * 4);
-  w.xfrag_bf16 = q;
-  q += ws_align256((size_t)(MT_MAX / 8) * XFRAG_WORDS_M * 4);
   w.xh_exp = reinterpret_cast<int*>(q);
   q += ws_align256(MT_MAX * 4);
   w.rt = reinterpret_cast<MedRoute*>(q);
@@ -619,7 +809,7 @@ MediumWs carve_medium_ws(void* ws) {
   return w;
 }
 static_assert(medium_ws_bytes() == ws_align256((size_t)MT_MAX * E * 2) + ws_align256((size_t)MT_MAX * H * 2) +
-                                       2 * ws_align256((size_t)(MT_MAX / 8) * XFRAG_WORDS_M * 4) +
+                                       ws_align256((size_t)(MT_MAX / 8) * XFRAG_WORDS_M * 4) +
                                        ws_align256(MT_MAX * 4) + ws_align256(sizeof(MedRoute)) +
                                        ws_align256((size_t)MPAIRS * I * 2) + ws_align256((size_t)MPAIRS * H * 4) + ws_align256((size_t)MT_MAX * H * 2),
               "medium workspace size and carve-up must agree");
@@ -631,14 +821,35 @@ cudaError_t medium_kernels_init() {
   return cudaFuncSetAttribute(mdown_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mdown_smem_bytes());
 }
 
-cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float eps, void* y, int32_t* ids_out,
-                                float* w_out, const MediumWs& ws, int sm_count, unsigned* err, cudaStream_t st,
-                                bool pdl_first) {
-  cudaError_t e = launch_router_chunks(L, x, T, eps, ws, st, pdl_first);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, const LayerArgs* next, int T, float eps, void* y,
+                                int32_t* ids_out, float* w_out, const MediumWs& ws, int sm_count, unsigned* err,
+                                cudaStream_t st, bool pdl_first) {
+  XhatOut xo;
+  xo.xh = static_cast<__nv_bfloat16*>(ws.xh_bf16);
+  xo.xfrag = static_cast<uint32_t*>(ws.xfrag_f16);
+  xo.xh_exp = ws.xh_exp;
+  cudaError_t e;
+  bool pdl = pdl_first;
+  if (x != nullptr) {
+    MNormParams np;
+    np.x = static_cast<const __nv_bfloat16*>(x);
+    np.norm_w = static_cast<const __nv_bfloat16*>(L.norm_w);
+    np.eps = eps;
+    np.o = xo;
+    if ((e = launch_pdl(mnorm_kernel, T, 256, 0, st, pdl, np)) != cudaSuccess) return e;
+    pdl = true;
+  }
+
+  MLogitsParams lp;
+  lp.wr = static_cast<const __nv_bfloat16*>(L.router_w);
+  lp.xh = xo.xh;
+  lp.T = T;
+  lp.logits = static_cast<__nv_bfloat16*>(ws.logits);
+  const int units = E * ((T + 7) / 8);
+  if ((e = launch_pdl(mlogits_kernel, std::min(units, 2 * sm_count), 256, 0, st, pdl, lp)) != cudaSuccess) return e;
 
   MRouteParams rp;
-  rp.logits = static_cast<const __nv_bfloat16*>(ws.logits);
+  rp.logits = lp.logits;
   rp.T = T;
   rp.rt = ws.rt;
   rp.ids_out = ids_out;
@@ -648,8 +859,8 @@ cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float 
   MGateUpParams gp;
   gp.experts = L.experts;
   gp.tscale = L.tscale;
-  gp.xfrag = static_cast<const uint32_t*>(ws.xfrag_f16);
-  gp.xh_exp = ws.xh_exp;
+  gp.xfrag = xo.xfrag;
+  gp.xh_exp = xo.xh_exp;
   gp.rt = ws.rt;
   gp.h = static_cast<__nv_bfloat16*>(ws.h);
   gp.err = err;
@@ -669,9 +880,12 @@ cudaError_t launch_medium_chain(const LayerArgs& L, const void* x, int T, float 
   MCombineParams cp;
   cp.rt = ws.rt;
   cp.part = ws.part;
-  cp.T = T;
   cp.y = static_cast<__nv_bfloat16*>(y);
-  return launch_pdl(mcombine_kernel, (T * (H / 4) + 255) / 256, 256, 0, st, true, cp);
+  cp.publish = next != nullptr;
+  cp.next_norm_w = next ? static_cast<const __nv_bfloat16*>(next->norm_w) : nullptr;
+  cp.eps = eps;
+  cp.o = xo;
+  return launch_pdl(mcombine_kernel, T, 256, 0, st, true, cp);
 }
 
 }  // namespace flint
