@@ -328,7 +328,7 @@ SOURCES = {
     "fused": [CSRC + "decode_fused.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
     "chain": [CSRC + "decode.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
     "prefill": [CSRC + "prefill.cu", CSRC + "tc05.cuh", CSRC + "flint_common.cuh"],
-    "medium": [CSRC + "medium.cu", CSRC + "decode.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
+    "medium": [CSRC + "medium.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
     "dense": [CSRC + "dense.cu", CSRC + "decode_common.cuh", CSRC + "flint_common.cuh"],
 }
 TRAFFIC_FILES = {
@@ -471,7 +471,8 @@ def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, w
     kind = "fused" if persistent else ("medium" if B > 8 else "chain")
     prof, prof_src = profiled_traffic(kind, name)
     traffic = round(float(prof["ratio"]) * bytes_per_layer * NL) if prof else None
-    launches = math.ceil(NL / FUSED_MAX_LAYERS) if persistent else (5 if B > 8 else 3) * NL
+    # medium: 5 kernels per sublayer, plus the first sublayer's RMSNorm step
+    launches = math.ceil(NL / FUSED_MAX_LAYERS) if persistent else (5 * NL + 1 if B > 8 else 3 * NL)
     return {
         "value": round(ms_per_step * 1000.0 / NL, 3),
         "unit": "us/layer",
@@ -481,8 +482,10 @@ def measure_stack(F, synth, torch, name: str, layers, steps: int, warmup: int, w
         "roofline": {
             "kernel": ("decode_fused_kernel: one persistent launch = the whole 47-sublayer step"
                        if persistent else
-                       "medium-batch step (router over 8-token chunks, routing tables, expert-grouped gate/up and "
-                       "down, combine: 5 kernels per sublayer, PDL-chained, one CUDA graph)" if B > 8 else
+                       "medium-batch step (logits over (8-token chunk, expert) units, routing tables, "
+                       "expert-grouped gate/up and down, combine that also normalises the next sublayer's input: "
+                       "5 kernels per sublayer plus the first sublayer's RMSNorm, PDL-chained, one CUDA graph)"
+                       if B > 8 else
                        "decode step (router + gate/up + down per sublayer, PDL-chained, one CUDA graph)"),
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(gbs / peak, 4), "peak_source": peak_src,
