@@ -360,26 +360,50 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   }
 
   if (warp == GU_PRODUCER_WARP) {
-    // The slot table is written before any routed tile is requested; a reader
-    // of it first waits on such a tile's barrier (or on a partial-sum barrier
-    // downstream of one), which orders the table writes before its reads.
-    // This kernel needs the experts and token masks, not the weights.
-    warp_slot_experts(R, B, lane);
-    if (lane == 0) {
-      for (int n = issued;; ++n) {
-        const int i = bid + n * G;
-        if (i >= n_items) break;
-        const int s = n % STAGES;
+    // The routed tiles are requested as soon as the selection is known.  Slot
+    // k >= 1 is the (k-1)-th expert of the union in ascending order: the lane
+    // holding that word of the union (lanes 0..7, a prefix count gives each
+    // word's first slot) finds the bit.  The slot table itself is built by
+    // the epilogue warps, its only readers.
+    const uint32_t m = lane < 8 ? R.umask[lane] : 0u;
+    const int cnt = __popc(m);
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    const int base = incl - cnt;
+    issued = __shfl_sync(0xffffffffu, issued, 0);  // the prologue's copies (lane 0)
+    for (int n = issued;; ++n) {
+      const int i = bid + n * G;
+      if (i >= n_items) break;
+      const int slot = i / GU_TILES;
+      int e = E;
+      if (slot > 0) {
+        const int k = slot - 1;
+        const bool own = lane < 8 && k >= base && k < incl;
+        uint32_t mm = m;
+        for (int r = own ? k - base : 0; r > 0; --r) mm &= mm - 1u;
+        const int el = own ? lane * 32 + __ffs(mm) - 1 : 0;
+        e = __shfl_sync(0xffffffffu, el, __ffs(__ballot_sync(0xffffffffu, own)) - 1);
+      }
+      const int s = n % STAGES;
+      int ok = 1;
+      if (lane == 0) {
         if (n >= STAGES && !mbar_wait(&empty[s], ((n / STAGES) - 1) & 1)) {
           atomicOr(p.err, ERR_WAIT_EMPTY);
-          break;
+          ok = 0;
+        } else {
+          mbar_arrive_expect_tx(&full[s], TILE);
+          bulk_g2s(stages + (size_t)s * TILE, p.experts + (size_t)e * F::EXPERT + (size_t)(i % GU_TILES) * TILE,
+                   TILE, &full[s], pol);
         }
-        const int e = R.slot_expert[i / GU_TILES];
-        mbar_arrive_expect_tx(&full[s], TILE);
-        bulk_g2s(stages + (size_t)s * TILE, p.experts + (size_t)e * F::EXPERT + (size_t)(i % GU_TILES) * TILE,
-                 TILE, &full[s], pol);
-        issued = n + 1;
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issued = n + 1;
+    }
+    if (lane == 0) {
       // Do not leave copies in flight: wait for the last use of every stage.
       for (int n = issued - STAGES; n < issued; ++n) {
         if (n < 0) continue;
@@ -433,6 +457,10 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
 
   // ---- epilogue warps: thread = (token ep_tk, gate/up row ep_row of the tile)
   const int et = tid - (GU_PRODUCER_WARP + 1) * 32;
+  // The slot table (experts and token masks; this kernel needs no weights),
+  // built while the first tiles are in flight.
+  if (et < 32) warp_slot_experts(R, B, lane);
+  named_bar_sync(1, 64);
   const int ep_tk = et >> 3, ep_row = et & 7;
   float xs = 1.f;  // 2^-exponent of token ep_tk (NVFP4)
   if (FMT == 0 && ep_tk < B) xs = exp2i(-__ldcg(p.xh_exp + ep_tk));
