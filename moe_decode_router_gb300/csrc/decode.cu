@@ -271,8 +271,9 @@ constexpr int TSCALE_WORDS = ((NE * 2 + 3) / 4) * 4;  // per-expert (gate/up, do
 template <int FMT, int STAGES>
 __host__ __device__ constexpr size_t gateup_smem_bytes() {
   // [stages][red ring GU_RED x 8 x 128 fp32][tensor scales][full, empty][rfull, rempty][pad 16][Routing]
+  // [first pair of each slot]
   return (size_t)STAGES * Fmt<FMT>::GU_TILE + GU_RED * 8 * 128 * 4 + TSCALE_WORDS * 4 + 2 * STAGES * 8 +
-         2 * GU_RED * 8 + 16 + sizeof(Routing);
+         2 * GU_RED * 8 + 16 + (sizeof(Routing) + 15) / 16 * 16 + MAX_SLOTS * 4;
 }
 
 // Items are (slot, row tile) pairs, item i = slot * 64 + tile; CTA b takes
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   uint64_t* rfull = empty + STAGES;
   uint64_t* rempty = rfull + GU_RED;
   Routing& R = *reinterpret_cast<Routing*>(reinterpret_cast<uint8_t*>(rempty + GU_RED) + 16);
+  int* slot_pair0 = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&R) + (sizeof(Routing) + 15) / 16 * 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, bid = blockIdx.x;
@@ -458,8 +460,26 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
   // ---- epilogue warps: thread = (token ep_tk, gate/up row ep_row of the tile)
   const int et = tid - (GU_PRODUCER_WARP + 1) * 32;
   // The slot table (experts and token masks; this kernel needs no weights),
-  // built while the first tiles are in flight.
-  if (et < 32) warp_slot_experts(R, B, lane);
+  // built while the first tiles are in flight, and the first pair of each
+  // slot: h is stored by pair (slot, token), numbered slot by slot and token
+  // by token, so the down kernel stages all of it with one copy.
+  if (et < 32) {
+    warp_slot_experts(R, B, lane);
+    const int n_slots_w = R.n_slots;
+    int run = 0;
+    for (int c0 = 0; c0 < n_slots_w; c0 += 32) {
+      const int u = c0 + lane;
+      const int cnt = u < n_slots_w ? __popc(R.slot_mask[u]) : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      if (u < n_slots_w) slot_pair0[u] = run + incl - cnt;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
   named_bar_sync(1, 64);
   const int ep_tk = et >> 3, ep_row = et & 7;
   float xs = 1.f;  // 2^-exponent of token ep_tk (NVFP4)
@@ -490,7 +510,8 @@ __global__ void __launch_bounds__(GU_THREADS, 1) gateup_kernel(const GateUpParam
       const float up = __fmul_rn(usum, f);
       const float silu = __fdiv_rn(gate, __fadd_rn(1.0f, expf(-gate)));
       const __nv_bfloat16 hv = __float2bfloat16_rn(__fmul_rn(silu, up));
-      p.h[((size_t)slot * BMAX + ep_tk) * I + tile * 8 + ep_row] = hv;
+      const int pair = slot_pair0[slot] + __popc(mask & ((1u << ep_tk) - 1u));
+      p.h[(size_t)pair * I + tile * 8 + ep_row] = hv;
       hm = fmaxf(hm, fabsf(__bfloat162float(hv)));
     }
     __syncwarp();
@@ -520,8 +541,6 @@ struct DownParams {
 
 constexpr int MAX_HPARTS = 512;
 
-constexpr int DN_BULK_H_MAX = 16;  // staged h rows up to which they come by bulk copies
-
 template <int NG>
 struct DnCfg {
   static constexpr int COMPUTE_WARPS = 2 * NG;  // NG slot groups x 2 K halves
@@ -531,13 +550,13 @@ struct DnCfg {
 template <int FMT, int STAGES, int NG>
 __host__ __device__ constexpr size_t down_smem_fixed() {
   // [stages][red (2NG) x 128 fp32][tensor scales][full, empty barriers, h barrier][hexp 8, misc 8 ints]
-  // [pidx][pair token][pair slot][Routing]
+  // [pidx][pair token][Routing]
   return (size_t)STAGES * Fmt<FMT>::DN_TILE + DnCfg<NG>::COMPUTE_WARPS * 128 * 4 + TSCALE_WORDS * 4 +
-         2 * STAGES * 8 + 8 + 64 + MAX_SLOTS * BMAX + 64 + 64 + sizeof(Routing);
+         2 * STAGES * 8 + 8 + 64 + MAX_SLOTS * BMAX + 64 + sizeof(Routing);
 }
 template <int FMT, int STAGES, int NG>
 size_t down_smem_bytes(int B) {
-  return ((down_smem_fixed<FMT, STAGES, NG>() + 15) / 16) * 16 + (size_t)(1 + TOPK) * B * HS_STRIDE * 2;
+  return ((down_smem_fixed<FMT, STAGES, NG>() + 15) / 16) * 16 + (size_t)(1 + TOPK) * B * I * 2;
 }
 
 // CTA r owns output rows 16r..16r+15.  Slot u is consumed by warp group
@@ -562,8 +581,7 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   int* misc = hexp + 8;                                  // [1] n_pairs
   uint8_t* pidx = reinterpret_cast<uint8_t*>(misc + 8);  // [MAX_SLOTS][8]
   uint8_t* psrc_tok = pidx + MAX_SLOTS * BMAX;           // [<= 56] token of pair
-  uint8_t* psrc_slot = psrc_tok + 64;                    // [<= 56] slot of pair
-  Routing& R = *reinterpret_cast<Routing*>(psrc_slot + 64);
+  Routing& R = *reinterpret_cast<Routing*>(psrc_tok + 64);
   uint16_t* hs = reinterpret_cast<uint16_t*>(smem + ((down_smem_fixed<FMT, STAGES, NG>() + 15) / 16) * 16);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -622,7 +640,6 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
           if ((m >> tk) & 1u) {
             pidx[u * BMAX + tk] = (uint8_t)pi;
             psrc_tok[pi] = (uint8_t)tk;
-            psrc_slot[pi] = (uint8_t)u;
             ++pi;
           }
         }
@@ -646,32 +663,16 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
   }
 
   pdl_wait();  // gate/up of this sublayer is complete: h and hmax_part are final
-  if (FMT == 0 && tid == NCW * 32 + 1) {
-    // HBM is idle now: every NVFP4 tile beyond the ring is asked into L2 at
-    // once, so the ring refills at L2 latency (BF16's 16 KB tiles would take
-    // most of L2 at 8 tokens; measured slower there).
-    for (int n = STAGES; n < n_slots; ++n)
-      bulk_prefetch_l2(p.experts + (size_t)R.slot_expert[n] * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE, TILE);
-  }
-
-  // One round trip: every h row is requested at once, together with the
-  // per-token maxima that set the f16 exponents.  A few rows go as one bulk
-  // copy each; with many, the copy engine's per-copy cost would dominate, so
-  // every thread requests 16-byte pieces instead.
-  const bool h_bulk = n_pairs <= DN_BULK_H_MAX;
-  if (h_bulk) {
-    if (tid == NCW * 32) {
-      const uint64_t hpol = l2_evict_last();
-      mbar_arrive_expect_tx(hbar, (uint32_t)(n_pairs * I * 2));
-      for (int pr = 0; pr < n_pairs; ++pr)
-        bulk_g2s(hs + (size_t)pr * HS_STRIDE, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I, I * 2, hbar,
-                 hpol);
-    }
-  } else {
-    for (int idx = tid; idx < n_pairs * 64; idx += NT) {
-      const int pr = idx >> 6, ch = idx & 63;
-      cp_async16(hs + (size_t)pr * HS_STRIDE + ch * 8, p.h + ((size_t)psrc_slot[pr] * BMAX + psrc_tok[pr]) * I + ch * 8);
-    }
+  // h is stored by pair in the order of pidx: all of it is one copy, issued
+  // first.  Then, with HBM idle, every NVFP4 tile beyond the ring is asked
+  // into L2 at once, so the ring refills at L2 latency (BF16's 16 KB tiles
+  // would take most of L2 at 8 tokens; measured slower there).
+  if (tid == NCW * 32) {
+    mbar_arrive_expect_tx(hbar, (uint32_t)(n_pairs * I * 2));
+    bulk_g2s(hs, p.h, (uint32_t)(n_pairs * I * 2), hbar, l2_evict_last());
+    if (FMT == 0)
+      for (int n = STAGES; n < n_slots; ++n)
+        bulk_prefetch_l2(p.experts + (size_t)R.slot_expert[n] * F::EXPERT + F::GU_BYTES + (size_t)rt * TILE, TILE);
   }
   if (FMT == 0 && warp < B) {
     float v[MAX_HPARTS / 32];
@@ -686,17 +687,13 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
     const unsigned mb = redux_max(__float_as_uint(m));
     if (lane == 0) hexp[warp] = f16_range_exp(__uint_as_float(mb));
   }
-  if (h_bulk) {
-    if (!mbar_wait(hbar, 0) && tid == 0) atomicOr(p.err, ERR_WAIT_FULL);
-  } else {
-    cp_async_wait_all();
-  }
+  if (!mbar_wait(hbar, 0) && tid == 0) atomicOr(p.err, ERR_WAIT_FULL);
   __syncthreads();
   if (FMT == 0) {
     // bf16 h -> f16 h * 2^hexp[token], in place (each thread its own chunks).
     for (int idx = tid; idx < n_pairs * 64; idx += NT) {
       const int pr = idx >> 6, ch = idx & 63;
-      uint4* ptr = reinterpret_cast<uint4*>(hs + (size_t)pr * HS_STRIDE + ch * 8);
+      uint4* ptr = reinterpret_cast<uint4*>(hs + (size_t)pr * I + ch * 8);
       float f[8];
       bf16x8_to_f32(*ptr, f);
       const float sc = exp2i(hexp[psrc_tok[pr]]);
@@ -755,7 +752,7 @@ __global__ void __launch_bounds__(DnCfg<NG>::THREADS, 1) down_kernel(const DownP
     const uint32_t mask = R.slot_mask[u];
     if (g < B && ((mask >> g) & 1u)) {
       const uint32_t* hr =
-          reinterpret_cast<const uint32_t*>(hs + (size_t)pidx[u * BMAX + g] * HS_STRIDE + kh * 256);
+          reinterpret_cast<const uint32_t*>(hs + (size_t)pidx[u * BMAX + g] * I + kh * 256);
 #pragma unroll
       for (int kb = 0; kb < 16; ++kb) {
         bfr[kb][0] = hr[kb * 8 + t];
