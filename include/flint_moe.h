@@ -137,11 +137,14 @@ int flint_moe_pack_weights(const flint_moe_dims *dims, const void *gate_up,
  * NVFP4 weights take one cooperative kernel, one thread block per SM (at
  * least 128 SMs, else FLINT_MOE_ERR_UNSUPPORTED), whose blocks exchange
  * logits, h and y through the workspace.  9 <= B <= 64 (NVFP4 only, else
- * FLINT_MOE_ERR_UNSUPPORTED) runs the medium-batch chain: the router over
- * chunks of 8 tokens; one block that builds the table of slot-chunks (an
- * expert with up to 16 of the tokens that selected it); gate/up and down
- * kernels that stream each selected expert's tiles once per slot-chunk; and
- * a kernel that adds the pairs' down projections in a fixed order.  Its
+ * FLINT_MOE_ERR_UNSUPPORTED) runs the medium-batch chain: one block per token
+ * for the RMSNorm; the router logits over (chunk of 8 tokens, expert) units;
+ * one block that selects every token's top-6 and builds the table of
+ * slot-chunks (an expert with up to 8 of the tokens that selected it);
+ * gate/up and down kernels that stream each selected expert's tiles once per
+ * slot-chunk; and one block per token that adds the pairs' down projections
+ * in a fixed order (inside a stack it also normalises the next sublayer's
+ * input, so that sublayer skips the RMSNorm block).  Its
  * workspace is flint_moe_workspace_bytes(dims, 64) bytes (less returns
  * FLINT_MOE_ERR_WORKSPACE).  B > 64 returns FLINT_MOE_ERR_UNSUPPORTED.  The
  * result is deterministic: the same inputs and kernel choice give the same
