@@ -47,7 +47,6 @@ struct RouterParams {
   float eps;
   int want_f16;
   __nv_bfloat16* logits;   // [B][E]
-  __nv_bfloat16* xh_bf16;  // [B][H] natural layout
   uint32_t* xfrag_f16;     // x_hat * 2^xh_exp[token] in f16, fragment order
   uint32_t* xfrag_bf16;    // x_hat in bf16, fragment order
   int* xh_exp;             // [B]
@@ -205,22 +204,26 @@ __global__ void __launch_bounds__(256, 2) router_kernel(const RouterParams p) {
     p.logits[(size_t)(tid % NB) * E + e0 + tid / NB] = __float2bfloat16_rn(cs_value(a));
   }
 
-  if (blockIdx.x == 0) {
-    // Every CTA computed the same x_hat; CTA 0 publishes it, natural and in
-    // fragment order.  Columns 8k..8k+7 are block kb = (k % 32) / 2, register
-    // r = k % 2 of K-slice k / 32, lanes 4t..4t+3 of token t.
-    const int ws = k0 >> 8, kb = (k0 & 255) >> 4, rr = (k0 >> 3) & 1;
+  // Every CTA computed the same x_hat.  CTA b < 8 publishes K-slice b
+  // (columns 256 b .. 256 b + 255, held by its warp b) in mma fragment order:
+  // columns 8k..8k+7 are block kb = (k % 32) / 2, register r = k % 2 of
+  // K-slice k / 32, lanes 4t..4t+3 of token t.  BF16 weights take x_hat in
+  // bf16; NVFP4 takes it in f16 scaled by 2^xh_exp[t], the exponent from the
+  // token's largest |x_hat|, which each publishing CTA reduces itself.  (One
+  // CTA publishing everything was the router's last CTA by 1.8 us at 8 tokens.)
+  if (blockIdx.x < 8) {
+    const int kb = (k0 & 255) >> 4, rr = (k0 >> 3) & 1;  // K-slice k0 >> 8 == warp
+    const bool mine = warp == (int)blockIdx.x;
+    if (!p.want_f16) {
+      if (mine) {
 #pragma unroll
-    for (int t = 0; t < NB; ++t) {
-      uint32_t pk[4];
+        for (int t = 0; t < NB; ++t)
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        pk[i] = (__float_as_uint(xv[t][2 * i]) >> 16) | (__float_as_uint(xv[t][2 * i + 1]) & 0xFFFF0000u);
-      *reinterpret_cast<uint4*>(p.xh_bf16 + (size_t)t * H + k0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) p.xfrag_bf16[((ws * 32 + 4 * t + i) * 16 + kb) * 2 + rr] = pk[i];
-    }
-    if (p.want_f16) {
+          for (int i = 0; i < 4; ++i)
+            p.xfrag_bf16[((warp * 32 + 4 * t + i) * 16 + kb) * 2 + rr] =
+                (__float_as_uint(xv[t][2 * i]) >> 16) | (__float_as_uint(xv[t][2 * i + 1]) & 0xFFFF0000u);
+      }
+    } else {
 #pragma unroll
       for (int t = 0; t < NB; ++t) {
         float m = 0.f;
@@ -230,16 +233,18 @@ __global__ void __launch_bounds__(256, 2) router_kernel(const RouterParams p) {
         if (lane == 0) atomicMax(&xmax[t], wm);
       }
       __syncthreads();
+      if (mine) {
 #pragma unroll
-      for (int t = 0; t < NB; ++t) {
-        const int ex = f16_range_exp(__uint_as_float(xmax[t]));
-        const float sc = exp2i(ex);
+        for (int t = 0; t < NB; ++t) {
+          const int ex = f16_range_exp(__uint_as_float(xmax[t]));
+          const float sc = exp2i(ex);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __half2 hv = __floats2half2_rn(__fmul_rn(xv[t][2 * i], sc), __fmul_rn(xv[t][2 * i + 1], sc));
-          p.xfrag_f16[((ws * 32 + 4 * t + i) * 16 + kb) * 2 + rr] = *reinterpret_cast<const uint32_t*>(&hv);
+          for (int i = 0; i < 4; ++i) {
+            const __half2 hv = __floats2half2_rn(__fmul_rn(xv[t][2 * i], sc), __fmul_rn(xv[t][2 * i + 1], sc));
+            p.xfrag_f16[((warp * 32 + 4 * t + i) * 16 + kb) * 2 + rr] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          if (blockIdx.x == 0 && lane == 0) p.xh_exp[t] = ex;
         }
-        if (tid == 0) p.xh_exp[t] = ex;
       }
     }
   }
@@ -937,7 +942,6 @@ cudaError_t launch_decode_chain(int fmt, const LayerArgs& L, const void* x, cons
   rp.eps = eps;
   rp.want_f16 = fmt == 0;
   rp.logits = static_cast<__nv_bfloat16*>(ws.logits);
-  rp.xh_bf16 = static_cast<__nv_bfloat16*>(ws.xh_bf16);
   rp.xfrag_f16 = static_cast<uint32_t*>(ws.xfrag_f16);
   rp.xfrag_bf16 = static_cast<uint32_t*>(ws.xfrag_bf16);
   rp.xh_exp = ws.xh_exp;
